@@ -1,0 +1,260 @@
+"""CPU oracle for the streamed QKV projection and packed rotated low-bit K/V
+attention -- TEST INFRASTRUCTURE.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline use this package.  The library never imports it, and it imports
+nothing from the library.  The arithmetic lives in ``kvq_oracle.c`` (plain C,
+built here with gcc); this module builds it and marshals numpy arrays.
+
+Arrays of BF16 or FP16 values are passed as ``uint16`` bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvq_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkvq_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+HD = 128
+
+
+def build(force: bool = False) -> str:
+    """Compile kvq_oracle.c into libkvq_oracle.so (gcc, -O2, no fast-math,
+    no FMA contraction, OpenMP when the compiler has it)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    try:
+        subprocess.run(base + ["-fopenmp", _SRC, "-o", tmp, "-lm"], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base + [_SRC, "-o", tmp, "-lm"], check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+            lib.kvqo_bf16_to_f32.restype = F
+            lib.kvqo_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.kvqo_f32_to_bf16.restype = ctypes.c_uint16
+            lib.kvqo_f32_to_bf16.argtypes = [F]
+            lib.kvqo_f16_to_f32.restype = F
+            lib.kvqo_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.kvqo_f32_to_f16.restype = ctypes.c_uint16
+            lib.kvqo_f32_to_f16.argtypes = [F]
+            lib.kvqo_rot_scale.restype = F
+            lib.kvqo_rot_scale.argtypes = []
+            lib.kvqo_rotate.restype = None
+            lib.kvqo_rotate.argtypes = [P, I64, P]
+            lib.kvqo_quant_head.restype = None
+            lib.kvqo_quant_head.argtypes = [P, I, I, P, P]
+            lib.kvqo_dequant_head.restype = None
+            lib.kvqo_dequant_head.argtypes = [P, P, I, I, P]
+            lib.kvqo_kv_rotate_quant_pack.restype = I
+            lib.kvqo_kv_rotate_quant_pack.argtypes = [P, I64, I, P, I64, I, I, P, P, P, P]
+            lib.kvqo_kv_unpack.restype = I
+            lib.kvqo_kv_unpack.argtypes = [P, P, P, P, I64, I, I, I, P]
+            lib.kvqo_qkv_proj.restype = I
+            lib.kvqo_qkv_proj.argtypes = [P, P, I, P, I64, I, I, P, P, F, P, P, P, P, P, P]
+            lib.kvqo_attention.restype = I
+            lib.kvqo_attention.argtypes = [P, I64, I, P, P, P, P, I64, I64, I, I, F, P, I64, P]
+            lib.kvqo_attention_mixed.restype = I
+            lib.kvqo_attention_mixed.argtypes = [P, I64, I, I, P, P, P, P, P, P, P, P, I, F, P, I64, P]
+            lib.kvqo_threads.restype = I
+            lib.kvqo_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def threads() -> int:
+    """OpenMP threads the oracle runs with."""
+    return int(_load().kvqo_threads())
+
+
+# ----------------------------------------------------------------- number formats
+def bf16_to_f32(bits) -> np.ndarray:
+    """BF16 bit patterns (uint16) -> float32, exactly."""
+    b = _c(bits, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    lib = _load()
+    x = _c(x, np.float32)
+    return np.array([lib.kvqo_f32_to_bf16(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def f32_to_f16(x) -> np.ndarray:
+    lib = _load()
+    x = _c(x, np.float32)
+    return np.array([lib.kvqo_f32_to_f16(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def f16_to_f32(h) -> np.ndarray:
+    lib = _load()
+    h = _c(h, np.uint16)
+    return np.array([lib.kvqo_f16_to_f32(int(v)) for v in h.ravel()], dtype=np.float32).reshape(h.shape)
+
+
+def rot_scale() -> float:
+    return float(_load().kvqo_rot_scale())
+
+
+# ----------------------------------------------------------------- rotation and quantiser
+def rotate(x) -> np.ndarray:
+    """x[..., 128] -> x . H (fp32, the FWHT order the format fixes)."""
+    x = _c(x, np.float32)
+    assert x.shape[-1] == HD
+    y = np.empty_like(x)
+    _load().kvqo_rotate(_p(x), x.size // HD, _p(y))
+    return y
+
+
+def quant_head(y, group: int, bits: int):
+    """One rotated head vector y[128] -> (codes bytes, fp16 scale bits)."""
+    y = _c(y, np.float32)
+    assert y.shape == (HD,)
+    codes = np.empty(HD * bits // 8, np.uint8)
+    scales = np.empty(HD // group, np.uint16)
+    _load().kvqo_quant_head(_p(y), group, bits, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequant_head(codes, scales, group: int, bits: int) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint16)
+    y = np.empty(HD, np.float32)
+    _load().kvqo_dequant_head(_p(codes), _p(scales), group, bits, _p(y))
+    return y
+
+
+# ----------------------------------------------------------------- a1 / a1b
+def kv_rotate_quant_pack(kv, rows=None, *, hidden: int, group: int = 32, bits: int = 4):
+    """kv: uint16 BF16 bits [n, >= 2*hidden] (K then V).  Returns compact
+    token-major (k_codes, v_codes, k_scales, v_scales) for `rows`:
+    codes [n_rows, heads, 128*bits/8] uint8, scales [n_rows, heads, 128/group] uint16."""
+    kv = _c(kv, np.uint16)
+    n, ld = kv.shape
+    rows = np.arange(n, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    heads = hidden // HD
+    kc = np.empty((len(rows), heads, HD * bits // 8), np.uint8)
+    vc = np.empty_like(kc)
+    ks = np.empty((len(rows), heads, HD // group), np.uint16)
+    vs = np.empty_like(ks)
+    rc = _load().kvqo_kv_rotate_quant_pack(_p(kv), ld, hidden, _p(rows), len(rows), group, bits,
+                                           _p(kc), _p(vc), _p(ks), _p(vs))
+    if rc:
+        raise ValueError("oracle kv_rotate_quant_pack: bad arguments")
+    return kc, vc, ks, vs
+
+
+def kv_unpack(kc, vc, ks, vs, *, group: int = 32, bits: int = 4) -> np.ndarray:
+    kc, vc = _c(kc, np.uint8), _c(vc, np.uint8)
+    ks, vs = _c(ks, np.uint16), _c(vs, np.uint16)
+    n_rows, heads = kc.shape[:2]
+    out = np.empty((n_rows, 2 * heads * HD), np.uint16)
+    rc = _load().kvqo_kv_unpack(_p(kc), _p(vc), _p(ks), _p(vs), n_rows, heads * HD, group, bits, _p(out))
+    if rc:
+        raise ValueError("oracle kv_unpack: bad arguments")
+    return out
+
+
+# ----------------------------------------------------------------- a2
+def qkv_proj(x, w, rows=None, *, group: int = 32, bits: int = 4, q_norm_w=None, k_norm_w=None, eps: float = 1e-6):
+    """x: uint16 BF16 bits [n, C]; w: uint16 BF16 bits [3C, C].  Returns a dict
+    with q_f32 [n_rows, C], q_bf16 [n_rows, C] (uint16) and compact
+    token-major k_codes, v_codes, k_scales, v_scales for `rows`."""
+    x, w = _c(x, np.uint16), _c(w, np.uint16)
+    n, C = x.shape
+    assert w.shape == (3 * C, C)
+    rows = np.arange(n, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    heads = C // HD
+    qn = None if q_norm_w is None else _c(q_norm_w, np.float32)
+    kn = None if k_norm_w is None else _c(k_norm_w, np.float32)
+    out = dict(
+        q_f32=np.empty((len(rows), C), np.float32),
+        q_bf16=np.empty((len(rows), C), np.uint16),
+        k_codes=np.empty((len(rows), heads, HD * bits // 8), np.uint8),
+        v_codes=np.empty((len(rows), heads, HD * bits // 8), np.uint8),
+        k_scales=np.empty((len(rows), heads, HD // group), np.uint16),
+        v_scales=np.empty((len(rows), heads, HD // group), np.uint16),
+    )
+    rc = _load().kvqo_qkv_proj(_p(x), _p(w), C, _p(rows), len(rows), group, bits, _p(qn), _p(kn), eps,
+                               _p(out["q_f32"]), _p(out["q_bf16"]), _p(out["k_codes"]), _p(out["v_codes"]),
+                               _p(out["k_scales"]), _p(out["v_scales"]))
+    if rc:
+        raise ValueError("oracle qkv_proj: bad arguments")
+    return out
+
+
+# ----------------------------------------------------------------- a4
+def attention(q, k_codes, v_codes, k_scales, v_scales, *, n_kv: int, group: int = 32, bits: int = 4,
+              sm_scale: float | None = None, rows=None) -> np.ndarray:
+    """q: uint16 BF16 bits [n_q, C] (rotated basis).  K/V store in the
+    library's head-major layout: codes [heads, n_pad, 128*bits/8] uint8,
+    scales [heads, n_pad, 128/group] uint16.  Returns fp32 [n_rows, C]."""
+    q = _c(q, np.uint16)
+    n_q, C = q.shape
+    heads = C // HD
+    kc, vc = _c(k_codes, np.uint8), _c(v_codes, np.uint8)
+    ks, vs = _c(k_scales, np.uint16), _c(v_scales, np.uint16)
+    n_pad = kc.shape[1]
+    assert kc.shape[0] == heads and ks.shape[:2] == (heads, n_pad)
+    rows = np.arange(n_q, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    sm = HD ** -0.5 if sm_scale is None else sm_scale
+    out = np.empty((len(rows), C), np.float32)
+    rc = _load().kvqo_attention(_p(q), C, heads, _p(kc), _p(vc), _p(ks), _p(vs), n_kv, n_pad, group, bits, sm,
+                                _p(rows), len(rows), _p(out))
+    if rc:
+        raise ValueError("oracle attention: bad arguments")
+    return out
+
+
+def attention_mixed(q, ranges, *, group: int = 32, sm_scale: float | None = None, rows=None) -> np.ndarray:
+    """ranges: list of dicts with start, len, bits and the range's own
+    head-major store (k_codes, v_codes, k_scales, v_scales; capacity = their
+    second dimension).  Ranges must tile [0, n_kv) in order."""
+    q = _c(q, np.uint16)
+    n_q, C = q.shape
+    heads = C // HD
+    rows = np.arange(n_q, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    sm = HD ** -0.5 if sm_scale is None else sm_scale
+    keep = []
+    arrs = {}
+    for key, dt in (("k_codes", np.uint8), ("v_codes", np.uint8), ("k_scales", np.uint16), ("v_scales", np.uint16)):
+        lst = [_c(r[key], dt) for r in ranges]
+        ptrs = (ctypes.c_void_p * len(lst))(*[a.ctypes.data for a in lst])
+        keep += lst + [ptrs]
+        arrs[key] = ctypes.cast(ptrs, ctypes.c_void_p)
+    starts = np.array([r["start"] for r in ranges], np.int64)
+    lens = np.array([r["len"] for r in ranges], np.int64)
+    bitss = np.array([r["bits"] for r in ranges], np.int32)
+    caps = np.array([_c(r["k_codes"], np.uint8).shape[1] for r in ranges], np.int64)
+    out = np.empty((len(rows), C), np.float32)
+    rc = _load().kvqo_attention_mixed(_p(q), C, heads, len(ranges), _p(starts), _p(lens), _p(bitss), _p(caps),
+                                      arrs["k_codes"], arrs["v_codes"], arrs["k_scales"], arrs["v_scales"],
+                                      group, sm, _p(rows), len(rows), _p(out))
+    if rc:
+        raise ValueError("oracle attention_mixed: bad arguments")
+    return out
