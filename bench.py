@@ -1,0 +1,383 @@
+"""Benchmark: one transformer block's streamed QKV projection + packed-INT4-K/V
+attention on the H3 Ref2VA-sized workload (N = 152,263 tokens, hidden 7168,
+56 heads x 128), on synthetic seeded inputs.
+
+One step = streamed_qkv_proj (x . W^T on the tensor cores, Q kept BF16 and
+rotated, K / V rotated, group-scaled (32) and packed to INT4) followed by
+packed_kv_attention (Q against the packed K/V, output written over Q).
+
+Prints one JSON line (rank 0).  `value` is block TFLOP/s:
+(2 N C 3C + 4 N^2 C) / step time, over all ranks.  Every rank runs an
+independent block (its own seed): the work per GPU is fixed (weak scaling)
+and no data crosses ranks; only the timings are reduced (max).
+
+--impl reference times the CPU oracle (the plain C reference implementation
+of the same computation) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "block TFLOP/s + tokens/s (QKV GEMM + INT4-KV attn) at N=152,263; peak GiB"
+GiB = 2.0 ** 30
+
+
+def flops(n: int, C: int) -> tuple[float, float]:
+    """(projection FLOPs, attention FLOPs) of one block."""
+    return 2.0 * n * C * 3 * C, 4.0 * n * n * C
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle (reference arm / baseline)
+class CpuOracleSample:
+    """The CPU oracle on a bounded sample of the block: the projection of
+    `proj_rows` token rows and the attention of `attn_rows` query rows (all
+    heads, all N keys).  Both are exact per row, so time per row extrapolates
+    to the whole block.  Inputs come from the seeded generators (generated
+    once, on the GPU when there is one, and copied to the host)."""
+
+    def __init__(self, wl, seed: int, proj_rows: int, attn_rows: int):
+        import oracle
+        from serving_tcgen05_streamed_gb300 import inputs
+
+        self.wl = wl
+        n, C = wl.n, wl.hidden
+        heads = C // 128
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        as_u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+        x, w, qn, kn = inputs.block_inputs(wl, device=dev)
+        rows = inputs.sample_rows(n, proj_rows, seed=seed).numpy()
+        self.xb = as_u16(x[torch.as_tensor(rows, device=dev)])
+        self.wb = as_u16(w)
+        self.qn = None if qn is None else qn.cpu().numpy()
+        self.kn = None if kn is None else kn.cpu().numpy()
+        del x, w
+        cap = ((n + 127) // 128) * 128
+        kc, vc, ks, vs = inputs.random_packed_kv(heads, n, cap, 32, 4, seed=seed, device=dev)
+        self.kc, self.vc, self.ks, self.vs = kc.cpu().numpy(), vc.cpu().numpy(), as_u16(ks), as_u16(vs)
+        del kc, vc, ks, vs
+        self.q = as_u16(inputs.random_q(attn_rows, C, seed=seed))
+        oracle.build()
+        self.cores = oracle.threads()
+        self.sample = (f"{proj_rows} projection rows + {attn_rows} attention query rows ({heads} heads x {n} keys); "
+                       f"time per row extrapolated to N={n}")
+
+    def run(self):
+        """Returns extrapolated block seconds."""
+        import oracle
+        n = self.wl.n
+        t0 = time.perf_counter()
+        oracle.qkv_proj(self.xb, self.wb, q_norm_w=self.qn, k_norm_w=self.kn)
+        t_proj = (time.perf_counter() - t0) / self.xb.shape[0]
+        t0 = time.perf_counter()
+        oracle.attention(self.q, self.kc, self.vc, self.ks, self.vs, n_kv=n)
+        t_attn = (time.perf_counter() - t0) / self.q.shape[0]
+        return t_proj * n + t_attn * n
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    cpu = CpuOracleSample(wl, seed=100, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
+    secs = []
+    for i in range(args.warmup + args.steps):
+        t = cpu.run()
+        if i >= args.warmup:
+            secs.append(t)
+    t_block = sum(secs) / len(secs)
+    v = sum(flops(wl.n, wl.hidden)) / t_block / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_block * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (fp64 accumulation)", "data": "synthetic (seeded generators)",
+        "config": {"workload": wl.name, "n_tokens": wl.n, "hidden": wl.hidden, "heads": wl.heads, "group": 32,
+                   "kv_bits": 4},
+        "tokens_per_s": wl.n / t_block,
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu.cores, "kind": "oracle", "sample": cpu.sample},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def peak_memory(wl, x, w, qn, kn, kvq):
+    """Peak bytes allocated by one streamed block (ours) and by the
+    materialise-BF16-QKV-then-quantise path, above the resident inputs."""
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    q, store = kvq.streamed_qkv_proj(x, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn)
+    kvq.packed_kv_attention(q, store, out=q)
+    torch.cuda.synchronize()
+    ours = torch.cuda.max_memory_allocated() - base
+    del q, store
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    qkv = x @ w.t()  # [N, 3C] BF16 materialised (cuBLAS)
+    C = wl.hidden
+    store = kvq.kv_rotate_quant_pack(qkv[:, C:], C, 32, 4)
+    torch.cuda.synchronize()
+    mat = torch.cuda.max_memory_allocated() - base
+    del qkv, store
+    torch.cuda.synchronize()
+    return ours / GiB, mat / GiB
+
+
+def run_gpu(args, wl, world, rank, local):
+    import serving_tcgen05_streamed_gb300 as kvq
+    from serving_tcgen05_streamed_gb300 import inputs
+
+    kvq.load()
+    n, C = wl.n, wl.hidden
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    x, w, qn, kn = inputs.block_inputs(wl, device=dev)
+    if world > 1:  # independent problems per rank
+        x = x.roll(rank * 7, dims=0)
+    fp, fa = flops(n, C)
+
+    peak_ours, peak_mat = peak_memory(wl, x, w, qn, kn, kvq)
+
+    q = torch.empty((n, C), dtype=torch.bfloat16, device=dev)
+    store = kvq.PackedKV.empty(n, C, 32, 4, dev)
+
+    def step():
+        kvq.streamed_qkv_proj(x, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q,
+                              store=store, stream=stream)
+        ev_a0.record(stream)
+        kvq.packed_kv_attention(q, store, out=q, stream=stream)
+        ev_a1.record(stream)
+
+    ev_a0, ev_a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert kvq.device_status() == kvq.KVQ_OK
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    attn_ms = []
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        ends[i].synchronize()
+        attn_ms.append(ev_a0.elapsed_time(ev_a1))
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(world, total_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * (fp + fa) / (ms_per_step * 1e-3) / 1e12
+    assert kvq.device_status() == kvq.KVQ_OK
+
+    # ------------------------------------------------------------ end to end: host buffers in and out
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty((n, C), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    e2e_steps = max(1, min(args.steps, 3))
+    for i in range(1 + e2e_steps):
+        if i == 1:
+            torch.cuda.synchronize()
+            barrier(world)
+            t0 = time.perf_counter()
+        x_dev.copy_(x_host, non_blocking=True)
+        kvq.streamed_qkv_proj(x_dev, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q,
+                              store=store, stream=stream)
+        kvq.packed_kv_attention(q, store, out=q, stream=stream)
+        out_host.copy_(q, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = max_over_ranks(world, e2e_s)
+    e2e_val = world * (fp + fa) / e2e_s / 1e12
+
+    # ------------------------------------------------------------ roofline of the dominant kernel (attention)
+    peaks, peak_kind = load_peaks()
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    attn_tflops = fa / (attn_avg_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            traffic = json.load(f).get("bytes_per_launch")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del x_host, out_host, x_dev
+        sample = CpuOracleSample(wl, seed=7, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
+        t_block = sample.run()
+        cpu = {"value": (fp + fa) / t_block / 1e12, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
+               "sample": sample.sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 GEMM / fp16 attention operands, fp32 accumulate",
+            "data": "synthetic (seeded generators; random-init weights of the H3 block shape)",
+            "config": {"workload": wl.name, "n_tokens": n, "hidden": C, "heads": wl.heads, "group": 32,
+                       "kv_bits": 4, "chunk_tokens": wl.chunk_tokens, "qk_rmsnorm": True,
+                       "l2": "inputs larger than L2 (x 2.04 GiB, packed K/V 1.14 GiB)",
+                       "parallelism": f"independent blocks x{world}"},
+            "tokens_per_s": world * n / (ms_per_step * 1e-3),
+            "kernel_ms": {"qkv_proj": ms_per_step - attn_avg_ms, "attention": attn_avg_ms},
+            "kernel_tflops": {"qkv_proj": fp / ((ms_per_step - attn_avg_ms) * 1e-3) / 1e12,
+                              "attention": attn_tflops},
+            "peak_gib": peak_ours, "peak_gib_materialise_bf16_qkv": peak_mat,
+            "peak_ratio": peak_ours / peak_mat if peak_mat else None,
+            "roofline": {"kernel": "packed_kv_attention", "bound": "tensor", "achieved": attn_tflops,
+                         "peak": peak, "unit": "TFLOP/s", "frac": attn_tflops / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} bf16 sustained (fp16 dense rate = bf16 dense rate)"},
+            "clocks": clocks,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(x.numel() * 2),
+                    "d2h_bytes_per_step": int(n * C * 2),
+                    "note": "x copied in from pinned host memory and the attention output copied back each step; "
+                            "W stays resident"},
+            "gpu_launches": 2 * args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--ref-proj-rows", type=int, default=16)
+    ap.add_argument("--ref-attn-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from serving_tcgen05_streamed_gb300 import inputs
+    wl = inputs.H3_REF2VA
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, wl, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    run_gpu(args, wl, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

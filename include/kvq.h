@@ -1,0 +1,188 @@
+/*
+ * kvq.h -- C ABI of the streamed QKV projection with rotated, group-scaled,
+ * packed low-bit K/V, and of the attention that reads that packed K/V.
+ *
+ * The operations follow the comfy-kitchen feature request "Streamed QKV
+ * Projection and Packed Low-Bit K/V Support for Extreme Long-Sequence
+ * Attention" (section "Proposed backend capability": a streamed/tiled QKV
+ * GEMM keeps Q in BF16/FP16 and sends K and V through rotate -> quantise ->
+ * packed 4-bit storage; attention consumes Q and the packed K/V and decodes
+ * K/V tile by tile; section "Dense fallback is important": no full BF16
+ * expansion of K/V; section "Mixed precision for conditioning": chosen token
+ * ranges at INT8).  The rotation, scaling and rounding conventions follow
+ * vram_lab.py ("VRAM Lab"): `_hadamard` (Sylvester Hadamard / sqrt(n)),
+ * `_fq_int4` (group absmax / 7, round half to even), `_Int8KV` (rotated INT8,
+ * absmax / 127; rotated-basis identities q.k = (qH).(kH), P.V = (P.(VH)).H^T).
+ *
+ * Conventions shared by every call
+ *  - head_dim is 128; hidden = heads * 128.
+ *  - H is the 128x128 Sylvester Hadamard matrix divided by sqrt(128); "rotate"
+ *    means x -> x.H computed as the fast Walsh-Hadamard transform with
+ *    butterfly strides 1, 2, ..., 64 in fp32, then one multiply by
+ *    fp32(1/sqrt(128)).  H is symmetric, so un-rotating is the same operation.
+ *  - Quantiser (per head, per group of `group` in {32, 64, 128} elements of
+ *    the rotated vector y): amax = max|y|; s = fp16_rn(amax / Q) with Q = 7
+ *    (bits 4) or 127 (bits 8); code = clamp(rint(y / float(s)), -Q, Q) (ties
+ *    to even, IEEE division), or 0 when s == 0.
+ *  - Packed store ("store"), one per K and one per V, HEAD-MAJOR:
+ *      codes  uint8 [heads][cap][128*bits/8]  (bits 4: element 2i in the low
+ *             nibble of byte i, 2i+1 in the high nibble, two's complement;
+ *             bits 8: one int8 per element)
+ *      scales fp16  [heads][cap][128/group]
+ *    For the single-precision calls cap = kvq_padded_rows(n) (n rounded up to
+ *    a multiple of 128); rows n..cap-1 are written as zero codes and scales.
+ *  - Q and attention outputs are token-major [n][hidden] with head h at
+ *    columns h*128 .. h*128+127; BF16 unless stated.
+ *  - All device pointers are caller-owned and must be 16-byte aligned.  The
+ *    library allocates no device memory and keeps no workspace.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *    and never synchronise.  Argument errors are reported before any launch;
+ *    launch failures return KVQ_ERR_CUDA.  Every device-side wait is bounded:
+ *    a wait that runs out sets a device error word that kvq_device_status()
+ *    reads, and the kernel returns early (its outputs are then undefined).
+ *  - Inputs must be finite, and rotated Q, K and V values must lie within the
+ *    fp16 range (|v| < 65504): the attention computes on fp16 operands.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t / CUstream). */
+typedef struct CUstream_st *kvq_stream_t;
+
+enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_ARG = 1,         /* a size, count or pointer argument is invalid */
+    KVQ_ERR_ALIGN = 2,       /* a pointer or leading dimension is not 16-byte aligned */
+    KVQ_ERR_UNSUPPORTED = 3, /* a valid but unsupported combination (e.g. causal) */
+    KVQ_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+    KVQ_ERR_TIMEOUT = 5      /* a device-side wait ran out (see kvq_device_status) */
+};
+
+#define KVQ_HEAD_DIM 128
+#define KVQ_ROW_TILE 128
+#define KVQ_MAX_RANGES 16
+
+/* Human-readable name of a status code (static storage). */
+KVQ_API const char *kvq_status_str(int status);
+
+/* Library version string (static storage). */
+KVQ_API const char *kvq_version(void);
+
+/* ---------------------------------------------------------------- sizes
+ * Byte sizes of the packed store ("Potential reduction": Q BF16 plus 4-bit
+ * K and V, plus quantisation metadata).  Pure host functions. */
+
+/* n rounded up to a multiple of KVQ_ROW_TILE (the row capacity `cap`). */
+KVQ_API int64_t kvq_padded_rows(int64_t n);
+/* Bytes of ONE codes array (K or V): heads * cap * 128 * bits / 8. */
+KVQ_API size_t kvq_codes_bytes(int64_t cap, int hidden, int bits);
+/* Bytes of ONE scales array (K or V): heads * cap * (128 / group) * 2. */
+KVQ_API size_t kvq_scales_bytes(int64_t cap, int hidden, int group);
+
+/* ---------------------------------------------------------------- a1: rotate + quantise + pack
+ * ("Quality-oriented low-bit format": Hadamard rotation, per-group scaling.)
+ * kv: BF16 [n][ld_kv] device; K = columns [0, hidden), V = [hidden, 2*hidden).
+ * Writes the K and V stores (cap = kvq_padded_rows(n), pad rows zeroed).
+ * group in {32, 64, 128}; bits in {4, 8}.  ld_kv >= 2*hidden, a multiple of 8.
+ * Codes and scales are bit-exact with the conventions above. */
+KVQ_API int kv_rotate_quant_pack(const void *kv, int64_t n, int hidden, int64_t ld_kv, int group, int bits, void *k_codes,
+                         void *v_codes, void *k_scales, void *v_scales, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------- a1b: unpack (diagnostic)
+ * Inverse of a1: dequantise (code * float(s)), un-rotate, round to BF16 into
+ * kv_out [n][ld_out] (K then V, as a1's input).  This materialises BF16 K/V
+ * by design; the attention never calls it. */
+KVQ_API int kv_unpack(const void *k_codes, const void *v_codes, const void *k_scales, const void *v_scales, int64_t n,
+              int hidden, int group, int bits, void *kv_out, int64_t ld_out, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------- a2: streamed fused QKV projection
+ * ("Proposed backend capability": streamed/tiled QKV GEMM; Q -> BF16,
+ * K and V -> rotate + quantise -> packed 4-bit.)
+ * x: BF16 [n][hidden]; w_qkv: BF16 [3*hidden][hidden] (rows [0,C) produce Q,
+ * [C,2C) K, [2C,3C) V; head h = 128 consecutive rows within each block).
+ * For each token: acc = x . w_qkv^T in fp32 on the tensor cores, then per head
+ *   Q: [RMSNorm with q_norm_w] -> rotate -> BF16 (round to nearest even) into q_out [n][hidden]
+ *   K: [RMSNorm with k_norm_w] -> rotate -> quantise/pack (bits 4) into the K store
+ *   V: rotate -> quantise/pack (bits 4) into the V store
+ * RMSNorm is v * (1/sqrt(mean(v^2) + eps)) * w over the head's 128 values,
+ * w a [128] fp32 device vector (NULL = no normalisation).  The rotation takes
+ * the fp32 accumulator directly.  Tokens are processed chunk by chunk in
+ * chunk_tokens-row chunks (0 = one chunk); results do not depend on the
+ * chunk size.  No [n][3*hidden] tensor and no BF16 K/V exist at any time.
+ * q_out must not alias x. */
+KVQ_API int streamed_qkv_proj(const void *x, const void *w_qkv, int64_t n, int hidden, int group, int64_t chunk_tokens,
+                      const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, void *k_codes,
+                      void *v_codes, void *k_scales, void *v_scales, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------- a4: packed-K/V attention
+ * ("Proposed backend capability": attention reads Q BF16 and packed INT4
+ * K/V, decoding K/V tile by tile; "Dense fallback is important".)
+ * q: BF16 [n_q][hidden], ROTATED basis (as written by streamed_qkv_proj).
+ * K/V stores: bits 4, cap = kvq_padded_rows(n_kv).  Non-causal softmax over
+ * all n_kv keys with scale sm_scale (<= 0 selects 1/sqrt(128)), then the
+ * output is un-rotated: out[i] = (sum_j p_ij v^_j / sum_j p_ij) . H, head by head.
+ * out: [n_q][hidden], BF16 (out_fp32 = 0) or fp32 (out_fp32 = 1).  With BF16
+ * output, out may equal q (each output row depends only on its own query
+ * row and every row is read before it is written by the same CTA).  */
+KVQ_API int packed_kv_attention(const void *q, int64_t n_q, const void *k_codes, const void *v_codes, const void *k_scales,
+                        const void *v_scales, int64_t n_kv, int hidden, int group, float sm_scale, int out_fp32,
+                        void *out, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------- a6: mixed precision by token range
+ * ("Mixed precision for conditioning": text / reference / audio ranges at
+ * INT8, generated video at rotated INT4.)  Every range holds its own K and V
+ * stores of `bits` (4 or 8) with row capacity `cap` (>= len, the head stride
+ * of its arrays); token t of the sequence is row t - start of the range that
+ * holds it.  Ranges must be given in order and tile [0, n) exactly, at most
+ * KVQ_MAX_RANGES of them.  INT8 ranges use the same rotation, so Q and the
+ * output need no per-range handling; rows len..cap-1 of a store are zeroed by
+ * the projection. */
+typedef struct kvq_range {
+    int64_t start;
+    int64_t len;
+    int64_t cap;
+    int32_t bits;
+    int32_t reserved;
+    void *k_codes;
+    void *v_codes;
+    void *k_scales;
+    void *v_scales;
+} kvq_range;
+
+KVQ_API int streamed_qkv_proj_mixed(const void *x, const void *w_qkv, int64_t n, int hidden, int group,
+                            int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
+                            void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream);
+
+KVQ_API int packed_kv_attention_mixed(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges, int hidden,
+                              int group, float sm_scale, int out_fp32, void *out, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------- device status
+ * Waits for `stream`, then returns KVQ_OK, or KVQ_ERR_TIMEOUT if a bounded
+ * device wait of any kernel of this library ran out since the last call
+ * (and clears the record), or KVQ_ERR_CUDA if the stream reports an error. */
+KVQ_API int kvq_device_status(kvq_stream_t stream);
+
+/* Self-test of the bounded wait: launches one block that waits on an
+ * mbarrier nothing ever arrives at, bounded by `ns` nanoseconds (at most
+ * 1e9); the wait runs out, the block records KVQ_ERR_TIMEOUT and returns.
+ * A following kvq_device_status() reports it.  Used by the test suite to
+ * show that a wait which cannot complete ends with a status, not a hang. */
+KVQ_API int kvq_selftest_wait_timeout(uint64_t ns, kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

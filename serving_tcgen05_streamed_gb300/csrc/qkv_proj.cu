@@ -1,0 +1,356 @@
+// qkv_proj.cu -- streamed fused QKV projection on the 5th-generation tensor
+// cores, with the Q / K / V epilogue fused in.
+//
+// The comfy-kitchen feature request ("Proposed backend capability") asks for
+// a streamed/tiled QKV GEMM that never materialises the full high-precision
+// [N, 3*hidden] output: Q is kept in BF16, K and V go through rotate ->
+// quantise -> packed 4-bit storage inside the projection.  vram_lab.py's
+// `_phase1_kv` fixes the fused row layout ([q | k | v], heads of 128
+// contiguous columns) and `_norm_rope` the per-head RMSNorm of Q and K.
+//
+// Design (one CTA per SM, persistent):
+//   tile       128 tokens x 256 output columns (two heads), K-step 64
+//   warp 0     TMA producer: x tile [128 x 64] and W tile [256 x 64] per
+//              stage, 128-byte swizzle, 4-stage shared-memory ring
+//   warp 1     TMEM allocator and MMA issuer: tcgen05.mma kind::f16
+//              M=128 N=256 K=16, fp32 accumulators in TMEM, two 256-column
+//              accumulators so the epilogue of one tile overlaps the main
+//              loop of the next
+//   warps 2-5  epilogue: one thread per token row reads a head's 128 fp32
+//              values from TMEM (tcgen05.ld 32x32b), applies RMSNorm (Q, K,
+//              optional), the 128-point rotation, and writes Q as BF16 or
+//              K / V as group-scaled INT4 / INT8 codes into the head-major
+//              store.  The accumulator never leaves the SM in fp32 or BF16.
+// Tiles are walked chunk by chunk (chunk_tokens rows at a time, rounded up
+// to whole 128-row tiles), columns-outer within a chunk, so that a chunk of
+// x and a few W column blocks stay in L2.  Every output element depends only
+// on its token row, so the results do not depend on the chunk size.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace kvq {
+namespace {
+
+__device__ unsigned int g_err_proj;
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* align slack */ + 256 /* barriers */;
+
+struct ProjParams {
+    int64_t n;
+    int hidden;
+    int m_tiles, n_tiles, k_blocks;
+    int chunk_m_tiles;
+    int64_t total_tiles;
+    const float *q_norm_w;
+    const float *k_norm_w;
+    float eps;
+    __nv_bfloat16 *q_out;
+    RangeTable ranges;
+};
+
+__device__ __forceinline__ void tile_coords(int64_t T, const ProjParams &p, int &m_idx, int &n_idx) {
+    const int64_t per_chunk = static_cast<int64_t>(p.chunk_m_tiles) * p.n_tiles;
+    const int64_t c = T / per_chunk;
+    const int64_t local = T - c * per_chunk;
+    const int m0 = static_cast<int>(c) * p.chunk_m_tiles;
+    const int mc = min(p.chunk_m_tiles, p.m_tiles - m0);
+    n_idx = static_cast<int>(local / mc);
+    m_idx = m0 + static_cast<int>(local % mc);
+}
+
+__device__ __forceinline__ void rmsnorm128(float (&v)[128], const float *__restrict__ w, float eps) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 128; i += 4) {
+        s0 = fmaf(v[i], v[i], s0);
+        s1 = fmaf(v[i + 1], v[i + 1], s1);
+        s2 = fmaf(v[i + 2], v[i + 2], s2);
+        s3 = fmaf(v[i + 3], v[i + 3], s3);
+    }
+    const float ms = ((s0 + s1) + (s2 + s3)) * (1.0f / 128.0f);
+    const float r = 1.0f / sqrtf(ms + eps);
+#pragma unroll
+    for (int i = 0; i < 128; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], r), __ldg(w + i));
+}
+
+template <int GROUP, int BITS>
+__device__ __forceinline__ void store_codes(const float (&v)[128], uint8_t *codes_row, uint16_t *scales_row) {
+    uint32_t words[128 * BITS / 32];
+    uint16_t sb[128 / GROUP];
+    quant128_thread<GROUP, BITS>(v, words, sb);
+    uint4 *dst = reinterpret_cast<uint4 *>(codes_row);
+#pragma unroll
+    for (int i = 0; i < 128 * BITS / 128; ++i)
+        dst[i] = make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]);
+    if constexpr (GROUP == 32) {
+        *reinterpret_cast<uint2 *>(scales_row) =
+            make_uint2(sb[0] | (static_cast<uint32_t>(sb[1]) << 16), sb[2] | (static_cast<uint32_t>(sb[3]) << 16));
+    } else if constexpr (GROUP == 64) {
+        *reinterpret_cast<uint32_t *>(scales_row) = sb[0] | (static_cast<uint32_t>(sb[1]) << 16);
+    } else {
+        *scales_row = sb[0];
+    }
+}
+
+template <int GROUP>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                    const __grid_constant__ ProjParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem_a = smem;
+    uint8_t *smem_b = smem + STAGES * A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 128);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_w);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (elect_one()) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0;  // bit s: stage s has been armed at least once
+            uint32_t armed_parity = 0;
+            for (int64_t T = blockIdx.x; T < p.total_tiles && !*abort_flag; T += gridDim.x) {
+                int m_idx, n_idx;
+                tile_coords(T, p, m_idx, n_idx);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_err_proj)) break;
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    tma_load_2d(smem_a + stage * A_BYTES, &tm_x, &full[stage], kb * BK, m_idx * BM);
+                    tma_load_2d(smem_b + stage * B_BYTES, &tm_w, &full[stage], kb * BK, n_idx * BN);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // drain: every copy this thread started has landed before the CTA exits
+            volatile int no_abort = 0;
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &no_abort, nullptr);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (elect_one()) {
+            constexpr uint32_t idesc = make_idesc_f16(BM, BN, 1);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool issued = false;
+            for (int64_t T = blockIdx.x; T < p.total_tiles && !*abort_flag; T += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, &g_err_proj)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, &g_err_proj)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem_a + stage * A_BYTES);
+                    const uint32_t b_addr = smem_u32(smem_b + stage * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        mma_f16_ss(d_tmem, make_sdesc_sw128(a_addr + k * 32), make_sdesc_sw128(b_addr + k * 32),
+                                   idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (issued && *abort_flag) {
+                // drain: wait until every MMA issued so far has completed
+                volatile int no_abort = 0;
+                uint64_t *drain = &tfull[acc];
+                mma_commit(drain);
+                mbar_wait(drain, acc_phase, &no_abort, nullptr);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int C = p.hidden;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t T = blockIdx.x; T < p.total_tiles && !*abort_flag; T += gridDim.x) {
+            int m_idx, n_idx;
+            tile_coords(T, p, m_idx, n_idx);
+            // warp-uniform before the warp-collective TMEM loads
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_err_proj))) break;
+            tc_fence_after();
+            const int64_t row = static_cast<int64_t>(m_idx) * BM + quarter * 32 + lane;
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j) {
+                uint32_t raw[128];
+                const uint32_t taddr = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + j * 128);
+                tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&raw[0]));
+                tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[32]));
+                tmem_ld32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&raw[64]));
+                tmem_ld32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&raw[96]));
+                tmem_ld_wait();
+                const int gcol = n_idx * BN + j * 128;
+                if (gcol >= 3 * C) continue;
+                float v[128];
+#pragma unroll
+                for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(raw[i]);
+                const int sect = gcol / C;
+                const int head = (gcol - sect * C) >> 7;
+                if (sect == 0) {
+                    if (p.q_norm_w) rmsnorm128(v, p.q_norm_w, p.eps);
+                    rotate128_thread(v);
+                    if (row < p.n) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.q_out + row * C + head * 128);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * k], v[8 * i + 2 * k + 1]);
+                                w4[k] = *reinterpret_cast<const uint32_t *>(&b2);
+                            }
+                            dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                    }
+                } else {
+                    if (sect == 1 && p.k_norm_w) rmsnorm128(v, p.k_norm_w, p.eps);
+                    rotate128_thread(v);
+                    // the range holding this token (rows past n belong to the last range's padding)
+                    int g = 0;
+                    for (int i = 1; i < p.ranges.n; ++i)
+                        if (row >= p.ranges.r[i].start) g = i;
+                    const RangeDev &R = p.ranges.r[g];
+                    const int64_t rr = row - R.start;
+                    if (rr < R.cap && (row < p.n || g == p.ranges.n - 1)) {
+                        const bool is_k = (sect == 1);
+                        if (R.bits == 4) {
+                            uint8_t *cr = (is_k ? R.k_codes : R.v_codes) + (head * R.cap + rr) * 64;
+                            uint16_t *sr = (is_k ? R.k_scales : R.v_scales) + (head * R.cap + rr) * (128 / GROUP);
+                            store_codes<GROUP, 4>(v, cr, sr);
+                        } else {
+                            uint8_t *cr = (is_k ? R.k_codes : R.v_codes) + (head * R.cap + rr) * 128;
+                            uint16_t *sr = (is_k ? R.k_scales : R.v_scales) + (head * R.cap + rr) * (128 / GROUP);
+                            store_codes<GROUP, 8>(v, cr, sr);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace
+
+int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int group, int64_t chunk_tokens,
+                    const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, const RangeTable &ranges,
+                    cudaStream_t s) {
+    alignas(64) CUtensorMap tm_x, tm_w;
+    if (encode_tmap_2d(&tm_x, x, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(n),
+                       static_cast<uint64_t>(hidden) * 2, BK, BM))
+        return KVQ_ERR_CUDA;
+    if (encode_tmap_2d(&tm_w, w, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(3) * hidden,
+                       static_cast<uint64_t>(hidden) * 2, BK, BN))
+        return KVQ_ERR_CUDA;
+    ProjParams p{};
+    p.n = n;
+    p.hidden = hidden;
+    p.m_tiles = static_cast<int>((n + BM - 1) / BM);
+    p.n_tiles = (3 * hidden + BN - 1) / BN;
+    p.k_blocks = hidden / BK;
+    int64_t cm = chunk_tokens <= 0 ? p.m_tiles : (chunk_tokens + BM - 1) / BM;
+    if (cm > p.m_tiles) cm = p.m_tiles;
+    p.chunk_m_tiles = static_cast<int>(cm);
+    p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    p.q_norm_w = q_norm_w;
+    p.k_norm_w = k_norm_w;
+    p.eps = eps;
+    p.q_out = static_cast<__nv_bfloat16 *>(q_out);
+    p.ranges = ranges;
+    const int grid = static_cast<int>(p.total_tiles < sm_count() ? p.total_tiles : sm_count());
+    cudaError_t e;
+    if (group == 32) {
+        e = cudaFuncSetAttribute(qkv_proj_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e == cudaSuccess) qkv_proj_kernel<32><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, p);
+    } else if (group == 64) {
+        e = cudaFuncSetAttribute(qkv_proj_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e == cudaSuccess) qkv_proj_kernel<64><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, p);
+    } else {
+        e = cudaFuncSetAttribute(qkv_proj_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e == cudaSuccess) qkv_proj_kernel<128><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, p);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return report_cuda(e, "projection launch");
+}
+
+cudaError_t read_clear_err_proj(unsigned int *v) {
+    cudaError_t e = cudaMemcpyFromSymbol(v, g_err_proj, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_err_proj, &zero, sizeof(unsigned int));
+}
+
+}  // namespace kvq

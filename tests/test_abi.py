@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/kvq.h declares, its size helpers reproduce the pages'
+memory arithmetic, and argument errors are reported before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import serving_tcgen05_streamed_gb300 as kvq
+from serving_tcgen05_streamed_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GiB = 2.0 ** 30
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = kvq.load()
+    declared = _declared()
+    assert declared == set(_lib.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert "sm_103a" in kvq.version()
+
+
+def _golden():
+    vals = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "pages_memory_arithmetic.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            name, v, tol = line.split()
+            vals[name] = (float(v), float(tol))
+    return vals
+
+
+def test_store_sizes_reproduce_the_pages_memory_arithmetic():
+    g = _golden()
+    n, C = int(g["tokens"][0]), int(g["hidden"][0])
+    cap = kvq.padded_rows(n)
+    assert cap == 152320 and cap % 128 == 0 and cap - n < 128
+    bf16_qkv = n * 3 * C * 2 / GiB
+    q = n * C * 2 / GiB
+    k = kvq.codes_bytes(cap, C, 4) / GiB
+    v = kvq.codes_bytes(cap, C, 4) / GiB
+    for name, val in (("bf16_qkv", bf16_qkv), ("q_bf16", q), ("k_4bit", k), ("v_4bit", v),
+                      ("qkv_packed_total", q + k + v)):
+        ref, tol = g[name]
+        assert abs(val - ref) <= tol, (name, val, ref)
+    # metadata: one fp16 scale per 32 elements per K and V
+    assert kvq.scales_bytes(cap, C, 32) == 56 * cap * 4 * 2
+    assert kvq.scales_bytes(cap, C, 128) == 56 * cap * 2
+    assert kvq.codes_bytes(cap, C, 8) == 2 * kvq.codes_bytes(cap, C, 4)
+    # invalid arguments give 0
+    assert kvq.codes_bytes(cap, 100, 4) == 0 and kvq.scales_bytes(cap, C, 48) == 0
+
+
+def test_status_strings():
+    assert kvq.status_str(kvq.KVQ_OK) == "ok"
+    assert "timed out" in kvq.status_str(kvq.KVQ_ERR_TIMEOUT)
+    assert kvq.status_str(99) == "unknown status"
+
+
+def test_argument_errors_are_reported_before_any_launch():
+    lib = kvq.load()
+    a16 = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails validation first
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    S = None
+    # null pointers / bad sizes
+    assert lib.kv_rotate_quant_pack(None, 10, 1024, 2048, 32, 4, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.kv_rotate_quant_pack(a16, 0, 1024, 2048, 32, 4, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.kv_rotate_quant_pack(a16, 10, 1000, 2048, 32, 4, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.kv_rotate_quant_pack(a16, 10, 1024, 2048, 48, 4, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.kv_rotate_quant_pack(a16, 10, 1024, 2048, 32, 2, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.kv_rotate_quant_pack(a16, 10, 1024, 2000, 32, 4, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ARG
+    # alignment
+    assert lib.kv_rotate_quant_pack(odd, 10, 1024, 2048, 32, 4, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ALIGN
+    assert lib.kv_rotate_quant_pack(a16, 10, 1024, 2052, 32, 4, a16, a16, a16, a16, S) == kvq.KVQ_ERR_ALIGN
+    assert lib.kv_unpack(a16, a16, a16, None, 10, 1024, 32, 4, a16, 2048, S) == kvq.KVQ_ERR_ARG
+    # projection
+    P = ctypes.c_void_p
+    assert lib.streamed_qkv_proj(a16, a16, 0, 1024, 32, 0, None, None, 1e-6, P(2 << 20), a16, a16, a16, a16, S) \
+        == kvq.KVQ_ERR_ARG
+    assert lib.streamed_qkv_proj(a16, a16, 10, 1024, 32, -1, None, None, 1e-6, P(2 << 20), a16, a16, a16, a16, S) \
+        == kvq.KVQ_ERR_ARG
+    assert lib.streamed_qkv_proj(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, a16, a16, a16, a16, a16, S) \
+        == kvq.KVQ_ERR_ARG  # q_out aliases x
+    assert lib.streamed_qkv_proj(a16, odd, 10, 1024, 32, 0, None, None, 1e-6, P(2 << 20), a16, a16, a16, a16, S) \
+        == kvq.KVQ_ERR_ALIGN
+    # attention
+    assert lib.packed_kv_attention(a16, 10, a16, a16, a16, a16, 0, 1024, 32, 0.0, 0, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.packed_kv_attention(a16, 10, a16, a16, a16, a16, 5, 1024, 32, 0.0, 2, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.packed_kv_attention(a16, 10, a16, a16, a16, a16, 5, 1024, 32, 0.0, 1, a16, S) == kvq.KVQ_ERR_ARG
+    assert lib.packed_kv_attention(a16, 10, a16, odd, a16, a16, 5, 1024, 32, 0.0, 0, a16, S) == kvq.KVQ_ERR_ALIGN
+    # mixed range tables: gaps, bad bits, capacity
+    R = _lib._Range
+    bad_gap = (R * 2)(R(0, 100, 128, 4, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20),
+                      R(101, 50, 128, 8, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20))
+    assert lib.packed_kv_attention_mixed(a16, 10, bad_gap, 2, 1024, 32, 0.0, 0, P(2 << 20), S) == kvq.KVQ_ERR_ARG
+    bad_bits = (R * 1)(R(0, 100, 128, 6, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20))
+    assert lib.packed_kv_attention_mixed(a16, 10, bad_bits, 1, 1024, 32, 0.0, 0, P(2 << 20), S) == kvq.KVQ_ERR_ARG
+    bad_cap = (R * 1)(R(0, 100, 100, 4, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20))
+    assert lib.packed_kv_attention_mixed(a16, 10, bad_cap, 1, 1024, 32, 0.0, 0, P(2 << 20), S) == kvq.KVQ_ERR_ARG
+    too_many = (R * 17)()
+    assert lib.packed_kv_attention_mixed(a16, 10, too_many, 17, 1024, 32, 0.0, 0, P(2 << 20), S) == kvq.KVQ_ERR_ARG
+    gap_proj = (R * 2)(R(0, 5, 128, 4, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20),
+                       R(5, 4, 128, 8, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20))
+    assert lib.streamed_qkv_proj_mixed(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, P(2 << 20), gap_proj, 2, S) \
+        == kvq.KVQ_ERR_ARG
+    assert lib.kvq_selftest_wait_timeout(0, S) == kvq.KVQ_ERR_ARG
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros((4, 256), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kvq.kv_rotate_quant_pack(x, 128)

@@ -1,0 +1,136 @@
+"""Parity of the streamed fused QKV projection (tcgen05 GEMM + rotate /
+quantise epilogue) with the CPU oracle.
+
+Tolerances: the GEMM accumulates in a different order from the oracle, so
+ - Q (BF16) must lie within one BF16 ulp of the oracle's fp32 value, plus an
+   absolute floor of 1e-4 x the RMS of that head's row for values near zero
+   (a different fp32 summation order over K <= 7168 terms moves the
+   accumulator by about sqrt(K) * 2^-24 of the terms' size, 20x below it);
+ - K / V codes may differ by at most 1, on at most 0.1% of the elements;
+ - scales must be equal except for at most 2% of the groups, which may
+   differ by one fp16 ulp (a relative accumulator difference d moves
+   fp16(amax/7) across a rounding boundary with probability about
+   2 * d * 2^11; with K = 7168 terms, x20 outlier channels and RMSNorm, d
+   reaches about 5e-6, i.e. about 2%).
+With inputs whose products and sums are exact (one-hot rows), everything is
+bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import serving_tcgen05_streamed_gb300 as kvq
+from serving_tcgen05_streamed_gb300 import inputs
+from tests._util import bf16_ulp, bits16, codes_as_int, to_token_major
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(q_gpu, store, ref, rows, bits=4, exact=False):
+    q = bits16(q_gpu[torch.as_tensor(rows, device=q_gpu.device)]).view(np.uint16)
+    qf = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if exact:
+        assert np.array_equal(q, ref["q_bf16"])
+    else:
+        err = np.abs(qf - ref["q_f32"])
+        rf = ref["q_f32"].astype(np.float64)
+        rms = np.sqrt(np.mean(rf.reshape(rf.shape[0], -1, 128) ** 2, axis=-1, keepdims=True))
+        floor = np.broadcast_to(1e-4 * rms, rms.shape[:2] + (128,)).reshape(rf.shape)
+        assert np.all(err <= bf16_ulp(rf) * 1.0001 + floor), float((err / bf16_ulp(rf)).max())
+    for cname, sname in (("k_codes", "k_scales"), ("v_codes", "v_scales")):
+        gc = to_token_major(getattr(store, cname), rows)
+        gs = to_token_major(getattr(store, sname), rows).view(np.uint16)
+        if exact:
+            assert np.array_equal(gc, ref[cname]), cname
+            assert np.array_equal(gs, ref[sname]), sname
+            continue
+        a, b = codes_as_int(gc, bits), codes_as_int(ref[cname], bits)
+        d = np.abs(a.astype(np.int32) - b)
+        assert d.max() <= 1, cname
+        assert np.mean(d != 0) <= 1e-3, (cname, float(np.mean(d != 0)))
+        ds = np.abs(gs.astype(np.int32) - ref[sname].astype(np.int32))
+        assert ds.max() <= 1, sname
+        assert np.mean(ds != 0) <= 2e-2, sname
+
+
+def _run(x, w, qn=None, kn=None, group=32, chunk=0):
+    q, store = kvq.streamed_qkv_proj(x.cuda(), w.cuda(), group=group, chunk_tokens=chunk,
+                                     q_norm_w=None if qn is None else qn.cuda(),
+                                     k_norm_w=None if kn is None else kn.cuda())
+    torch.cuda.synchronize()
+    assert kvq.device_status() == kvq.KVQ_OK
+    return q, store
+
+
+def test_tiny_block_full():
+    x, w, _, _ = inputs.block_inputs(inputs.TINY)
+    q, store = _run(x, w)
+    ref = oracle.qkv_proj(bits16(x), bits16(w))
+    _compare(q, store, ref, np.arange(x.shape[0]))
+    for t in (store.k_codes, store.v_codes):
+        assert int(t[:, x.shape[0]:].count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_one_hot_rows_are_bit_exact(group):
+    # x rows = +-2^e * e_k: every accumulator is one exact product, so Q, the
+    # codes and the scales must match the oracle bit for bit
+    n, C = 700, 768
+    g = torch.Generator().manual_seed(group)
+    x = torch.zeros((n, C))
+    k = torch.randint(0, C, (n,), generator=g)
+    sgn = torch.randint(0, 2, (n,), generator=g) * 2 - 1
+    e = torch.randint(-3, 4, (n,), generator=g).float()
+    x[torch.arange(n), k] = sgn * 2.0 ** e
+    x = x.to(torch.bfloat16)
+    w = (torch.randn((3 * C, C), generator=g) * 0.1).to(torch.bfloat16)
+    q, store = _run(x, w, group=group)
+    ref = oracle.qkv_proj(bits16(x), bits16(w), group=group)
+    _compare(q, store, ref, np.arange(n), exact=True)
+
+
+@pytest.mark.parametrize("n,C", [(1, 256), (129, 384), (1000, 1024)])
+def test_ragged_sizes_and_odd_head_counts(n, C):
+    g = torch.Generator().manual_seed(n)
+    x = torch.randn((n, C), generator=g).to(torch.bfloat16)
+    w = (torch.randn((3 * C, C), generator=g) * C ** -0.5).to(torch.bfloat16)
+    q, store = _run(x, w)
+    ref = oracle.qkv_proj(bits16(x), bits16(w))
+    _compare(q, store, ref, np.arange(n))
+
+
+def test_results_do_not_depend_on_chunk_size():
+    x, w, _, _ = inputs.block_inputs(inputs.TINY)
+    q0, s0 = _run(x, w, chunk=0)
+    for chunk in (128, 384, 1000):
+        q1, s1 = _run(x, w, chunk=chunk)
+        assert torch.equal(q0, q1)
+        for a, b in ((s0.k_codes, s1.k_codes), (s0.v_codes, s1.v_codes), (s0.k_scales, s1.k_scales),
+                     (s0.v_scales, s1.v_scales)):
+            assert torch.equal(a, b)
+
+
+def test_h3_block_with_rmsnorm_sampled_rows():
+    # H3 width (7168, 56 heads), Q/K RMSNorm, chunk 4096; the oracle checks sampled rows
+    wl = inputs.MID
+    x, w, qn, kn = inputs.block_inputs(wl)
+    q, store = _run(x, w, qn, kn, chunk=wl.chunk_tokens)
+    rows = inputs.sample_rows(wl.n, 40, seed=4).numpy()
+    ref = oracle.qkv_proj(bits16(x), bits16(w), rows, q_norm_w=qn.numpy(), k_norm_w=kn.numpy(), eps=1e-6)
+    _compare(q, store, ref, rows)
+
+
+@pytest.mark.slow
+def test_h3_ref2va_full_size_sampled_rows():
+    # the headline size, N = 152,263 (ragged tail of 71 rows), as the benchmark runs it
+    wl = inputs.H3_REF2VA
+    x, w, qn, kn = inputs.block_inputs(wl, device="cuda")
+    q, store = kvq.streamed_qkv_proj(x, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn)
+    torch.cuda.synchronize()
+    assert kvq.device_status() == kvq.KVQ_OK
+    rows = inputs.sample_rows(wl.n, 24, seed=5).numpy()
+    xs = x[torch.as_tensor(rows, device="cuda")]  # rows are independent: the oracle sees only the samples
+    ref = oracle.qkv_proj(bits16(xs), bits16(w), q_norm_w=qn.cpu().numpy(), k_norm_w=kn.cpu().numpy())
+    _compare(q, store, ref, rows)
+    # pad rows of the last tile are zero
+    assert int(store.k_codes[:, wl.n:].count_nonzero()) == 0
