@@ -310,11 +310,16 @@ def run_gpu(args, wl, world, rank, local):
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     attn_tflops = fa / (attn_avg_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    traffic = None
+    traffic = None  # DRAM bytes per launch from an ncu capture of the same attention source, else null
     tp = os.path.join(ROOT, "profiles", "attention_traffic.json")
     if os.path.exists(tp):
+        import hashlib
         with open(tp) as f:
-            traffic = json.load(f).get("bytes_per_launch")
+            rec = json.load(f)
+        src = os.path.join(ROOT, "serving_tcgen05_streamed_gb300", "csrc", "attention.cu")
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() == rec.get("source_sha256"):
+                traffic = rec.get("bytes_per_launch")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -332,7 +337,8 @@ def run_gpu(args, wl, world, rank, local):
             "data": "synthetic (seeded generators; random-init weights of the H3 block shape)",
             "config": {"workload": wl.name, "n_tokens": n, "hidden": C, "heads": wl.heads, "group": 32,
                        "kv_bits": 4, "chunk_tokens": wl.chunk_tokens, "qk_rmsnorm": True,
-                       "l2": "inputs larger than L2 (x 2.04 GiB, packed K/V 1.14 GiB)",
+                       "l2": f"inputs larger than L2 (x {n * C * 2 / GiB:.2f} GiB, packed K/V "
+                             f"{store.nbytes() / GiB:.2f} GiB)",
                        "parallelism": f"independent blocks x{world}"},
             "tokens_per_s": world * n / (ms_per_step * 1e-3),
             "kernel_ms": {"qkv_proj": ms_per_step - attn_avg_ms, "attention": attn_avg_ms},
@@ -363,11 +369,13 @@ def main():
     ap.add_argument("--ref-proj-rows", type=int, default=16)
     ap.add_argument("--ref-attn-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("h3_ref2va", "mid"), default="h3_ref2va",
+                    help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from serving_tcgen05_streamed_gb300 import inputs
-    wl = inputs.H3_REF2VA
+    wl = inputs.H3_REF2VA if args.workload == "h3_ref2va" else inputs.MID
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, wl, int(os.environ.get("WORLD_SIZE", "1")), rank)
