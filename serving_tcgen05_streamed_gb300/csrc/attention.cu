@@ -9,27 +9,36 @@
 // output is un-rotated once; `_online_combine` is the log-sum-exp merge that
 // the running softmax below performs tile by tile.
 //
-// One CTA = one head x 128 query rows.  Roles (9 warps):
-//   warps 0-3  dequantisers: per 128-key tile, load the INT4 / INT8 codes and
-//              fp16 scales straight from global memory (one tile ahead, in
-//              registers), decode them with integer bit tricks into FP16
+// One CTA = one head x 256 query rows, as two 128-row tiles A and B that
+// take turns on the tensor core (ping-pong): while the softmax of tile A
+// works on its scores, the tensor core runs tile B's P.V and next Q.K^T, and
+// the other way round.  16 warps in four warpgroups:
+//   WG0, WG1   softmax of tile A / B: one thread per query row; reads the S
+//              row from TMEM, keeps a running max in the log2 domain and
+//              rescales the output accumulator only when the row max grew by
+//              more than 2^8 (the stale max is used consistently for P and the
+//              row sum, so the result is exact); writes P as FP16 back into
+//              the first 64 TMEM columns of its own S, and at the end divides
+//              by the row sum, un-rotates the row with the 128-point fast
+//              Walsh-Hadamard transform in registers and stores it.
+//   WG2        dequantisers: per 128-key tile, load the INT4 / INT8 codes and
+//              fp16 scales straight from global memory (issued one tile
+//              ahead), decode them with integer bit tricks into FP16
 //              (code * scale) and store K^ [key][dim] and V^T [dim][key] in
 //              the 128-byte-swizzled K-major layout the tensor core reads.
 //              K^'s dims are permuted inside each 8-dim chunk (the order
 //              e0 e4 e1 e5 e2 e6 e3 e7 falls out of the nibble decode); Q is
 //              permuted the same way when it is converted, so Q.K^T is
-//              unchanged.  They also convert the BF16 Q tile to FP16 once.
-//   warps 4-7  softmax: one thread per query row; reads the S row from TMEM,
-//              keeps a running max in the log2 domain and rescales the
-//              output accumulator only when the max grows by more than 2^8
-//              (the stale max is used consistently for P and the row sum, so
-//              the result is exact); writes P as FP16 (to TMEM or shared
-//              memory), and at the end divides by the row sum, un-rotates
-//              the row with the 128-point fast Walsh-Hadamard transform in
-//              registers and stores it.
-//   warp 8     TMA of the Q tile, TMEM allocation, and the single MMA thread:
-//              S_j = Q.K^_j^T (M=128 N=128 K=128, two S buffers so S_{j+1}
-//              runs while the softmax works on S_j) and O += P_j.V^_j.
+//              unchanged.  They also convert the BF16 Q tiles to FP16 once.
+//   WG3        warp 12: TMA of the Q tiles, TMEM allocation and the single
+//              MMA thread; warps 13-15 idle.
+// Registers are redistributed with setmaxnreg: 176 per softmax thread, 104
+// per dequantiser, 56 for WG3 (512 threads x 128 at launch).
+// TMEM (512 columns): S_A, S_B, O_A, O_B, 128 columns each; P_t aliases the
+// first 64 columns of S_t.  tcgen05.mma instructions from one thread execute
+// in issue order, so S_t(j+1), issued after P_t(j).V^(j), overwrites P_t(j)
+// only after that MMA has read it; and the commit that signals S_t(j+1) also
+// covers P_t(j).V^(j), so O_t is final for tile j when the softmax sees S_t(j+1).
 // Scores, the softmax and O are fp32; the MMA operands are FP16 (11-bit
 // significand: the rotation spreads values evenly, where BF16's 8 bits would
 // cost a noticeably higher error floor).  No split over keys: every query
@@ -51,18 +60,24 @@ namespace {
 
 __device__ unsigned int g_err_attn;
 
-constexpr int BQ = 128;       // query rows per CTA
-constexpr int BKV = 128;      // keys per tile
-constexpr int KV_STAGES = 2;  // K^ / V^T shared-memory stages
+constexpr int BQT = 128;       // query rows per tile
+constexpr int NQT = 2;         // query tiles per CTA
+constexpr int BQ = BQT * NQT;  // query rows per CTA
+constexpr int BKV = 128;       // keys per tile
+constexpr int KV_STAGES = 2;   // K^ / V^T shared-memory stages
 constexpr int NUM_DQ_THREADS = 128;
-constexpr int NUM_SM_THREADS = 128;
-constexpr int NUM_THREADS = 288;
+constexpr int NUM_SM_THREADS = 128;  // per query tile
+constexpr int NUM_THREADS = 512;
+constexpr int WARP_MMA = 12;
+constexpr int REG_SOFTMAX = 176, REG_DEQUANT = 104, REG_MMA = 56;
+static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_DEQUANT + 128 * REG_MMA <= NUM_THREADS * 128,
+              "register split exceeds the launch budget");
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128x128 fp16 operand tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// TMEM columns
-constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_P0 = 256, TM_P1 = 320, TM_O = 384;
+__host__ __device__ constexpr uint32_t tm_s(int t) { return static_cast<uint32_t>(t * 128); }
+__host__ __device__ constexpr uint32_t tm_o(int t) { return static_cast<uint32_t>(256 + t * 128); }
 
 struct AttnParams {
     int64_t n_q;
@@ -75,13 +90,11 @@ struct AttnParams {
     int tiles_before[KVQ_MAX_RANGES + 1];
 };
 
-template <bool P_TMEM>
 struct SmemLayout {
-    static constexpr int Q = 0;
-    static constexpr int K = Q + TILE_BYTES;
-    static constexpr int V = K + KV_STAGES * TILE_BYTES;
-    static constexpr int P = V + KV_STAGES * TILE_BYTES;
-    static constexpr int BAR = P + (P_TMEM ? 0 : 2 * TILE_BYTES);
+    static constexpr int Q = 0;                           // NQT tiles
+    static constexpr int K = Q + NQT * TILE_BYTES;        // KV_STAGES tiles
+    static constexpr int V = K + KV_STAGES * TILE_BYTES;  // KV_STAGES tiles
+    static constexpr int BAR = V + KV_STAGES * TILE_BYTES;
     static constexpr int BYTES = BAR + 256 + 1024;
 };
 
@@ -126,8 +139,8 @@ constexpr uint32_t H2_NEG1152 = 0xE480E480u;  // (-1152, -1152)
 // FP16 pairs (e0,e4) (e1,e5) (e2,e6) (e3,e7), each times the scale pair s2.
 __device__ __forceinline__ void dq_int4_word(uint32_t w, uint32_t s2, uint32_t (&o)[4]) {
     const uint32_t w8 = w >> 8;
-    const uint32_t t0 = lop_and_xor(w, 0x000F000Fu, 0x64086408u);   // 1024 + (c0 + 8)
-    const uint32_t t1 = lop_and_xor(w, 0x00F000F0u, 0x64806480u);   // 1024 + 16 (c1 + 8)
+    const uint32_t t0 = lop_and_xor(w, 0x000F000Fu, 0x64086408u);  // 1024 + (c0 + 8)
+    const uint32_t t1 = lop_and_xor(w, 0x00F000F0u, 0x64806480u);  // 1024 + 16 (c1 + 8)
     const uint32_t t2 = lop_and_xor(w8, 0x000F000Fu, 0x64086408u);
     const uint32_t t3 = lop_and_xor(w8, 0x00F000F0u, 0x64806480u);
     o[0] = h2_mul(h2_add(t0, H2_NEG1032), s2);
@@ -144,6 +157,45 @@ __device__ __forceinline__ uint32_t dq_int8_pair(uint32_t a, uint32_t b, uint32_
 __device__ __forceinline__ uint32_t h2_dup(uint16_t s) { return static_cast<uint32_t>(s) * 0x10001u; }
 __device__ __forceinline__ uint32_t h2_pack(uint16_t lo, uint16_t hi) {
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // The tile sequence walks the ranges in order; tile j of the sequence is
@@ -167,10 +219,10 @@ __device__ __forceinline__ TileRef tile_ref(const AttnParams &p, int j) {
 // Raw codes a dequantiser thread holds for one tile (MIXED = INT8 possible).
 template <bool MIXED>
 struct RawTile {
-    uint4 k[MIXED ? 8 : 4];                           // one key row: 64 (INT4) or 128 (INT8) bytes
+    uint4 k[MIXED ? 8 : 4];                                     // one key row: 64 (INT4) or 128 (INT8) bytes
     typename std::conditional<MIXED, uint4, uint2>::type v[8];  // 8 keys x 16 dims (8 B INT4, 16 B INT8)
-    uint16_t ks[4];                                   // scales of the key row (128/GROUP used)
-    uint16_t vs[8];                                   // scale of each of the 8 keys for the 16-dim block
+    uint16_t ks[4];                                             // scales of the key row (128/GROUP used)
+    uint16_t vs[8];                                             // scale of each of the 8 keys, 16-dim block
     int bits;
 };
 
@@ -182,8 +234,7 @@ __device__ __forceinline__ void load_raw(const AttnParams &p, int head, int j, i
     R.bits = bits;
     const int cb = bits == 4 ? 64 : 128;
     constexpr int SG = 128 / GROUP;
-    // K unit: key row tid
-    {
+    {  // K unit: key row tid
         const int r = tid;
         if (r < t.valid) {
             const int64_t row = static_cast<int64_t>(head) * rg.cap + t.key0 + r;
@@ -201,8 +252,7 @@ __device__ __forceinline__ void load_raw(const AttnParams &p, int head, int j, i
             for (int g = 0; g < SG; ++g) R.ks[g] = 0;
         }
     }
-    // V unit: keys 8*kb .. 8*kb+7, dims 16*db .. 16*db+15
-    {
+    {  // V unit: keys 8*kb .. 8*kb+7, dims 16*db .. 16*db+15
         const int kb = tid & 15, db = tid >> 4;
         const int g = (16 * db) / GROUP;
 #pragma unroll
@@ -231,8 +281,7 @@ __device__ __forceinline__ void load_raw(const AttnParams &p, int head, int j, i
 
 template <int GROUP, bool MIXED>
 __device__ __forceinline__ void store_tile(const RawTile<MIXED> &R, uint8_t *k_tile, uint8_t *v_tile, int tid) {
-    // K^ row tid: 16 chunks of 8 dims (permuted e0 e4 e1 e5 e2 e6 e3 e7)
-    {
+    {  // K^ row tid: 16 chunks of 8 dims (permuted e0 e4 e1 e5 e2 e6 e3 e7)
         const int r = tid;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -252,77 +301,74 @@ __device__ __forceinline__ void store_tile(const RawTile<MIXED> &R, uint8_t *k_t
             *reinterpret_cast<uint4 *>(k_tile + sw128_off(r, c)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
-    // V^T rows 16*db .. 16*db+15, chunk kb (keys 8kb .. 8kb+7, natural order)
-    {
+    {  // V^T rows 16*db .. 16*db+15, chunk kb (keys 8kb .. 8kb+7, natural order)
         const int kb = tid & 15, db = tid >> 4;
-        uint32_t out[16][4];  // [dim][key pair]
+        uint32_t s2[4];
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-            const uint32_t s2 = h2_pack(R.vs[2 * kp], R.vs[2 * kp + 1]);
-            const auto a = R.v[2 * kp];
-            const auto b = R.v[2 * kp + 1];
-            if (!MIXED || R.bits == 4) {
-                // dims 0-7 from .x words, 8-15 from .y words
+        for (int kp = 0; kp < 4; ++kp) s2[kp] = h2_pack(R.vs[2 * kp], R.vs[2 * kp + 1]);
+        if (!MIXED || R.bits == 4) {
 #pragma unroll
-                for (int hw = 0; hw < 2; ++hw) {
-                    const uint32_t aw = hw ? a.y : a.x, bw = hw ? b.y : b.x;
-                    const uint32_t lo = prmt(aw, bw, 0x5410u);  // dims 0-3 of a | of b
-                    const uint32_t hi = prmt(aw, bw, 0x7632u);  // dims 4-7
+            for (int q = 0; q < 4; ++q) {  // dims 4q .. 4q+3 of the 16-dim block
+                uint32_t out[4][4];         // [dim][key pair]
+#pragma unroll
+                for (int kp = 0; kp < 4; ++kp) {
+                    const uint32_t aw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp])[q >> 1];
+                    const uint32_t bw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp + 1])[q >> 1];
+                    // low half: 4 dims of key a, high half: the same 4 dims of key a+1
+                    const uint32_t x = prmt(aw, bw, (q & 1) ? 0x7632u : 0x5410u);
                     uint32_t o[4];
-                    dq_int4_word(lo, s2, o);  // (d0) (d1) ... as pairs (a, b): o[0]=d0 o[1]=d1 o[2]=d2 o[3]=d3
-                    out[8 * hw + 0][kp] = o[0];
-                    out[8 * hw + 1][kp] = o[1];
-                    out[8 * hw + 2][kp] = o[2];
-                    out[8 * hw + 3][kp] = o[3];
-                    dq_int4_word(hi, s2, o);
-                    out[8 * hw + 4][kp] = o[0];
-                    out[8 * hw + 5][kp] = o[1];
-                    out[8 * hw + 6][kp] = o[2];
-                    out[8 * hw + 7][kp] = o[3];
-                }
-            } else {
+                    dq_int4_word(x, s2[kp], o);
 #pragma unroll
-                for (int d = 0; d < 16; ++d) {
-                    const uint32_t aw = reinterpret_cast<const uint32_t *>(&a)[d >> 2];
-                    const uint32_t bw = reinterpret_cast<const uint32_t *>(&b)[d >> 2];
-                    const uint32_t bi = static_cast<uint32_t>(d & 3);
-                    out[d][kp] = dq_int8_pair(aw, bw, bi | ((4u + bi) << 8), s2);
+                    for (int d = 0; d < 4; ++d) out[d][kp] = o[d];
                 }
+#pragma unroll
+                for (int d = 0; d < 4; ++d)
+                    *reinterpret_cast<uint4 *>(v_tile + sw128_off(16 * db + 4 * q + d, kb)) =
+                        make_uint4(out[d][0], out[d][1], out[d][2], out[d][3]);
             }
-        }
+        } else {
 #pragma unroll
-        for (int d = 0; d < 16; ++d) {
-            const int row = 16 * db + d;
-            *reinterpret_cast<uint4 *>(v_tile + sw128_off(row, kb)) =
-                make_uint4(out[d][0], out[d][1], out[d][2], out[d][3]);
+            for (int d = 0; d < 16; ++d) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int kp = 0; kp < 4; ++kp) {
+                    const uint32_t aw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp])[d >> 2];
+                    const uint32_t bw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp + 1])[d >> 2];
+                    const uint32_t bi = static_cast<uint32_t>(d & 3);
+                    w4[kp] = dq_int8_pair(aw, bw, bi | ((4u + bi) << 8), s2[kp]);
+                }
+                *reinterpret_cast<uint4 *>(v_tile + sw128_off(16 * db + d, kb)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
         }
     }
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+    tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+    tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+    tmem_ld32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+    tmem_ld32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+    tmem_ld_wait();
 }
 
-template <int GROUP, bool P_TMEM, bool MIXED>
+template <int GROUP, bool MIXED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttnParams p) {
-    using L = SmemLayout<P_TMEM>;
+    using L = SmemLayout;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = smem + L::Q;
     uint8_t *sK = smem + L::K;
     uint8_t *sV = smem + L::V;
-    uint8_t *sP = smem + L::P;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
     uint64_t *q_tma = bars + 0;
     uint64_t *q_ready = bars + 1;
-    uint64_t *kv_full = bars + 2;   // [2]
-    uint64_t *kv_empty = bars + 4;  // [2]
-    uint64_t *s_full = bars + 6;    // [2]
-    uint64_t *p_full = bars + 8;    // [2]
-    uint64_t *pv_done = bars + 10;
+    uint64_t *kv_full = bars + 2;   // [KV_STAGES]
+    uint64_t *kv_empty = bars + 4;  // [KV_STAGES]
+    uint64_t *s_full = bars + 6;    // [NQT]
+    uint64_t *p_full = bars + 8;    // [NQT]
+    uint64_t *pv_done = bars + 10;  // [NQT]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -334,17 +380,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_tma, 1);
         mbar_init(q_ready, NUM_DQ_THREADS);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KV_STAGES; ++i) {
             mbar_init(&kv_full[i], NUM_DQ_THREADS);
             mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < NQT; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], NUM_SM_THREADS);
+            mbar_init(&pv_done[i], 1);
         }
-        mbar_init(pv_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == WARP_MMA) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -353,71 +401,88 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
-        // ------------------------------------------------------------ Q load + MMA issue
-        if (elect_one()) {
-            prefetch_tmap(&tm_q);
-            mbar_arrive_expect_tx(q_tma, TILE_BYTES);
-            tma_load_2d(sQ, &tm_q, q_tma, head * 128, static_cast<int>(q0));
-            tma_load_2d(sQ + HALF_BYTES, &tm_q, q_tma, head * 128 + 64, static_cast<int>(q0));
-            constexpr uint32_t idesc = make_idesc_f16(128, 128, 0);
-            bool ok = mbar_wait(q_ready, 0, abort_flag, &g_err_attn);
-            tc_fence_after();
-            const uint32_t qa = smem_u32(sQ);
-            for (int j = 0; ok && j <= T; ++j) {
-                if (j < T) {
-                    const int st = j % KV_STAGES;
-                    if (!mbar_wait(&kv_full[st], (j / KV_STAGES) & 1, abort_flag, &g_err_attn)) break;
-                    tc_fence_after();
-                    const uint32_t kb = smem_u32(sK + st * TILE_BYTES);
-                    const uint32_t d = tmem + ((j & 1) ? TM_S1 : TM_S0);
+    if (warp >= 12) {
+        setmaxnreg_dec<REG_MMA>();
+        // ------------------------------------------------------------ WG3: Q load + MMA issue
+        if (warp == WARP_MMA) {
+            if (elect_one()) {
+                prefetch_tmap(&tm_q);
+                mbar_arrive_expect_tx(q_tma, NQT * TILE_BYTES);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                        mma_f16_ss(d, make_sdesc_sw128(qa + off), make_sdesc_sw128(kb + off), idesc, k > 0);
-                    }
-                    mma_commit(&s_full[j & 1]);
+                for (int t = 0; t < NQT; ++t) {
+                    const int y = static_cast<int>(q0) + t * BQT;
+                    tma_load_2d(sQ + t * TILE_BYTES, &tm_q, q_tma, head * 128, y);
+                    tma_load_2d(sQ + t * TILE_BYTES + HALF_BYTES, &tm_q, q_tma, head * 128 + 64, y);
                 }
-                if (j > 0) {
-                    const int jp = j - 1;
-                    const int st = jp % KV_STAGES;
-                    if (!mbar_wait(&p_full[jp & 1], (jp >> 1) & 1, abort_flag, &g_err_attn)) break;
-                    tc_fence_after();
-                    const uint32_t vb = smem_u32(sV + st * TILE_BYTES);
-                    const uint32_t d = tmem + TM_O;
+                constexpr uint32_t idesc = make_idesc_f16(128, 128, 0);
+                const uint32_t qa = smem_u32(sQ);
+                bool ok = mbar_wait(q_ready, 0, abort_flag, &g_err_attn);
+                tc_fence_after();
+                auto issue_s = [&](int j, int t) {  // S_t(j) = Q_t . K^_j^T
+                    const uint32_t kb = smem_u32(sK + (j % KV_STAGES) * TILE_BYTES);
+                    const uint32_t d = tmem + tm_s(t);
+                    const uint32_t q = qa + t * TILE_BYTES;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                        if constexpr (P_TMEM) {
-                            const uint32_t pa = tmem + ((jp & 1) ? TM_P1 : TM_P0) + k * 8;
-                            mma_f16_ts(d, pa, make_sdesc_sw128(vb + off), idesc, (jp > 0 || k > 0) ? 1u : 0u);
-                        } else {
-                            const uint32_t pa = smem_u32(sP + (jp & 1) * TILE_BYTES);
-                            mma_f16_ss(d, make_sdesc_sw128(pa + off), make_sdesc_sw128(vb + off), idesc,
-                                       (jp > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ss(d, make_sdesc_sw128(q + off), make_sdesc_sw128(kb + off), idesc, k > 0);
+                    }
+                    mma_commit(&s_full[t]);
+                };
+                if (ok && T > 0) {
+                    ok = mbar_wait(&kv_full[0], 0, abort_flag, &g_err_attn);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(0, 0);
+                        issue_s(0, 1);
+                    }
+                }
+                for (int j = 0; ok && j < T; ++j) {
+                    const int st = j % KV_STAGES;
+                    const uint32_t vb = smem_u32(sV + st * TILE_BYTES);
+                    for (int t = 0; t < NQT && ok; ++t) {
+                        // O_t += P_t(j) . V^_j, P_t read from TMEM (the first 64 columns of S_t)
+                        ok = mbar_wait(&p_full[t], j & 1, abort_flag, &g_err_attn);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
+                            mma_f16_ts(tmem + tm_o(t), tmem + tm_s(t) + k * 8, make_sdesc_sw128(vb + off), idesc,
+                                       (j > 0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&pv_done[t]);
+                        if (t == NQT - 1) mma_commit(&kv_empty[st]);
+                        if (j + 1 < T) {
+                            if (t == 0) {
+                                ok = mbar_wait(&kv_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, abort_flag,
+                                               &g_err_attn);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            issue_s(j + 1, t);
                         }
                     }
-                    mma_commit(pv_done);
-                    mma_commit(&kv_empty[st]);
                 }
+                // drain: nothing this thread issued is still running when the CTA exits
+                volatile int no_abort = 0;
+                if (*abort_flag) {
+                    mma_commit(&pv_done[0]);
+                    mbar_wait(&pv_done[0], 0, &no_abort, nullptr, 1000000000ull);
+                }
+                mbar_wait(q_tma, 0, &no_abort, nullptr);
             }
-            // drain: nothing this thread issued is still running when the CTA exits
-            volatile int no_abort = 0;
-            if (*abort_flag) {
-                mma_commit(&kv_empty[0]);
-                mbar_wait(&kv_empty[0], 0, &no_abort, nullptr, 1000000000ull);
-            }
-            mbar_wait(q_tma, 0, &no_abort, nullptr);
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ dequantisers
-        const int tid = threadIdx.x;  // 0..127
+    } else if (warp >= 8) {
+        setmaxnreg_dec<REG_DEQUANT>();
+        // ------------------------------------------------------------ WG2: dequantisers
+        const int tid = threadIdx.x - 256;  // 0..127
         // Q: BF16 -> FP16 in place, dims permuted e0 e4 e1 e5 e2 e6 e3 e7 within each 8-chunk
-        bool ok = mbar_wait(q_tma, 0, abort_flag, &g_err_attn);
+        const bool ok = mbar_wait(q_tma, 0, abort_flag, &g_err_attn);
         if (ok) {
 #pragma unroll 4
-            for (int i = tid; i < 2048; i += NUM_DQ_THREADS) {
+            for (int i = tid; i < NQT * TILE_BYTES / 16; i += NUM_DQ_THREADS) {
                 uint4 *c = reinterpret_cast<uint4 *>(sQ + i * 16);
                 const uint4 v = *c;
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -438,50 +503,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
         }
         mbar_arrive(q_ready);
-        RawTile<MIXED> cur, nxt;
-        if (ok && T > 0) load_raw<GROUP, MIXED>(p, head, 0, tid, nxt);
+        RawTile<MIXED> raw;
+        if (ok && T > 0) load_raw<GROUP, MIXED>(p, head, 0, tid, raw);
         for (int j = 0; ok && j < T && !*abort_flag; ++j) {
-            cur = nxt;
-            if (j + 1 < T) load_raw<GROUP, MIXED>(p, head, j + 1, tid, nxt);
             const int st = j % KV_STAGES;
             if (!mbar_wait(&kv_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, &g_err_attn)) break;
-            store_tile<GROUP, MIXED>(cur, sK + st * TILE_BYTES, sV + st * TILE_BYTES, tid);
+            store_tile<GROUP, MIXED>(raw, sK + st * TILE_BYTES, sV + st * TILE_BYTES, tid);
             fence_proxy_async_smem();
             mbar_arrive(&kv_full[st]);
+            if (j + 1 < T) load_raw<GROUP, MIXED>(p, head, j + 1, tid, raw);
         }
-    } else if (warp < 8) {
-        // ------------------------------------------------------------ softmax + epilogue
+    } else {
+        setmaxnreg_inc<REG_SOFTMAX>();
+        // ------------------------------------------------------------ WG0 / WG1: softmax + epilogue
+        const int t = warp >> 2;  // query tile
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // query row inside the tile
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t sa = tmem + lane_base + tm_s(t);
+        const uint32_t oa = tmem + lane_base + tm_o(t);
         float m = -INFINITY;  // running max (log2 units, possibly stale)
         float l = 0.0f;       // running sum of p
         const float sl = p.scale_log2;
         bool ok = true;
         for (int j = 0; j < T; ++j) {
-            const int b = j & 1;
             // the wait result is made warp-uniform before any warp-collective TMEM access
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, &g_err_attn))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, &g_err_attn))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sa = tmem + lane_base + (b ? TM_S1 : TM_S0);
+            uint32_t sr[128];
+            tmem_ld128(sa, sr);
             const int valid = tile_ref(p, j).valid;
-            // pass 1: row max of the scores
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 64) {
-                uint32_t r0[32], r1[32];
-                tmem_ld32(sa + c0, r0);
-                tmem_ld32(sa + c0 + 32, r1);
-                tmem_ld_wait();
+            if (valid < BKV) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (c0 + i < valid) mx = fmaxf(mx, __uint_as_float(r0[i]));
-                    if (c0 + 32 + i < valid) mx = fmaxf(mx, __uint_as_float(r1[i]));
-                }
+                for (int c = 0; c < 128; ++c)
+                    if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
             }
+            float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+#pragma unroll
+            for (int c = 2; c < 126; c += 4) {
+                mx0 = fmax3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            }
+            const float mx = fmax3(mx0, mx1, fmaxf(__uint_as_float(sr[126]), __uint_as_float(sr[127])));
             // Lazy rescaling: a row moves its max only when it grew by more than the
             // threshold, a decision that depends on that row's scores alone.  The
             // O rescale uses warp-collective TMEM loads and stores, so it runs for
@@ -494,87 +560,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 m = cand;
             }
             const bool rescale = __any_sync(0xffffffffu, grow);
-            l *= alpha;
-            // pass 2: p = 2^(s*sl - m) as FP16 pairs, and their row sum
+            // p = 2^(s*sl - m) as FP16 pairs, packed over S's first 64 columns
+            const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m, -m);
+            uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
             uint32_t pk[64];
-            float lsum = 0.0f;
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t r0[32];
-                tmem_ld32(sa + c0, r0);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float s0 = (c0 + i < valid) ? __uint_as_float(r0[i]) : -INFINITY;
-                    const float s1 = (c0 + i + 1 < valid) ? __uint_as_float(r0[i + 1]) : -INFINITY;
-                    const __half2 h = __floats2half2_rn(ex2_approx(fmaf(s0, sl, -m)), ex2_approx(fmaf(s1, sl, -m)));
-                    pk[(c0 + i) >> 1] = *reinterpret_cast<const uint32_t *>(&h);
-                    // the row sum uses the same FP16-rounded weights the MMA sees
-                    const float2 hf = __half22float2(h);
-                    lsum += hf.x + hf.y;
-                }
+            for (int c = 0; c < 128; c += 4) {
+                const uint64_t a0 = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2, nm2);
+                const uint64_t a1 =
+                    f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2, nm2);
+                float x0, x1, x2, x3;
+                f2_unpack(a0, x0, x1);
+                f2_unpack(a1, x2, x3);
+                const __half2 h0 = __floats2half2_rn(ex2_approx(x0), ex2_approx(x1));
+                const __half2 h1 = __floats2half2_rn(ex2_approx(x2), ex2_approx(x3));
+                pk[c >> 1] = *reinterpret_cast<const uint32_t *>(&h0);
+                pk[(c >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+                // the row sum uses the same FP16-rounded weights the MMA sees
+                const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+                acc0 = f2_add(acc0, f2_pack(f0.x, f0.y));
+                acc1 = f2_add(acc1, f2_pack(f1.x, f1.y));
             }
-            l += lsum;
-            // PV_{j-1} must be complete before O is touched and before P buffer (j&1) is reused
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort_flag, &g_err_attn))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (rescale) {
-                    const uint32_t oa = tmem + lane_base + TM_O;
+            float u0, u1, u2, u3;
+            f2_unpack(acc0, u0, u1);
+            f2_unpack(acc1, u2, u3);
+            l = l * alpha + ((u0 + u1) + (u2 + u3));
+            // S_t(j) completing implies P_t(j-1).V^(j-1) completed: O_t is final for j-1
+            if (rescale && j > 0) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t o32[32];
-                        tmem_ld32(oa + c0, o32);
-                        tmem_ld_wait();
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t o32[32];
+                    tmem_ld32(oa + c0, o32);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
-                        tmem_st16(oa + c0, *reinterpret_cast<const uint32_t(*)[16]>(&o32[0]));
-                        tmem_st16(oa + c0 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o32[16]));
-                    }
+                    for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+                    tmem_st16(oa + c0, *reinterpret_cast<const uint32_t(*)[16]>(&o32[0]));
+                    tmem_st16(oa + c0 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o32[16]));
                 }
             }
-            if constexpr (P_TMEM) {
-                const uint32_t pa = tmem + lane_base + (b ? TM_P1 : TM_P0);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_st16(pa + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
-                tmem_st_wait();
-            } else {
-                if (rescale) tmem_st_wait();
-                uint8_t *pt = sP + b * TILE_BYTES;
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    *reinterpret_cast<uint4 *>(pt + sw128_off(r, c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                fence_proxy_async_smem();
-            }
+            for (int c = 0; c < 4; ++c) tmem_st16(sa + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[b]);
+            mbar_arrive(&p_full[t]);
         }
         // epilogue: O / l, un-rotate, store
-        if (ok && T > 0 && __all_sync(0xffffffffu, mbar_wait(pv_done, (T - 1) & 1, abort_flag, &g_err_attn))) {
+        if (ok && T > 0 && __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (T - 1) & 1, abort_flag, &g_err_attn))) {
             tc_fence_after();
             uint32_t oraw[128];
-            const uint32_t oa = tmem + lane_base + TM_O;
-            tmem_ld32(oa + 0, *reinterpret_cast<uint32_t(*)[32]>(&oraw[0]));
-            tmem_ld32(oa + 32, *reinterpret_cast<uint32_t(*)[32]>(&oraw[32]));
-            tmem_ld32(oa + 64, *reinterpret_cast<uint32_t(*)[32]>(&oraw[64]));
-            tmem_ld32(oa + 96, *reinterpret_cast<uint32_t(*)[32]>(&oraw[96]));
-            tmem_ld_wait();
+            tmem_ld128(oa, oraw);
             const float inv_l = 1.0f / l;
             float o[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) o[c] = __uint_as_float(oraw[c]) * inv_l;
             rotate128_thread(o);
-            const int64_t row = q0 + r;
+            const int64_t row = q0 + t * BQT + r;
             if (row < p.n_q) {
                 if (p.out_fp32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * p.hidden + head * 128);
+                    float4 *dst =
+                        reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * p.hidden + head * 128);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    for (int i = 0; i < 32; ++i)
+                        dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                 } else {
                     uint4 *dst =
                         reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + row * p.hidden + head * 128);
@@ -596,13 +643,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 8) tmem_dealloc(tmem, 512);
+    if (warp == WARP_MMA) tmem_dealloc(tmem, 512);
 }
 
-template <int GROUP, bool P_TMEM, bool MIXED>
+template <int GROUP, bool MIXED>
 int launch_one(const CUtensorMap &tm, const AttnParams &p, dim3 grid, cudaStream_t s) {
-    constexpr int smem = SmemLayout<P_TMEM>::BYTES;
-    auto fn = attention_kernel<GROUP, P_TMEM, MIXED>;
+    constexpr int smem = SmemLayout::BYTES;
+    auto fn = attention_kernel<GROUP, MIXED>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) {
         fn<<<grid, NUM_THREADS, smem, s>>>(tm, p);
@@ -612,9 +659,8 @@ int launch_one(const CUtensorMap &tm, const AttnParams &p, dim3 grid, cudaStream
 }
 
 template <int GROUP>
-int launch_group(const CUtensorMap &tm, const AttnParams &p, dim3 grid, bool mixed, bool p_tmem, cudaStream_t s) {
-    if (mixed) return p_tmem ? launch_one<GROUP, true, true>(tm, p, grid, s) : launch_one<GROUP, false, true>(tm, p, grid, s);
-    return p_tmem ? launch_one<GROUP, true, false>(tm, p, grid, s) : launch_one<GROUP, false, false>(tm, p, grid, s);
+int launch_group(const CUtensorMap &tm, const AttnParams &p, dim3 grid, bool mixed, cudaStream_t s) {
+    return mixed ? launch_one<GROUP, true>(tm, p, grid, s) : launch_one<GROUP, false>(tm, p, grid, s);
 }
 
 }  // namespace
@@ -623,7 +669,7 @@ int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int h
                      int out_fp32, void *out, cudaStream_t s) {
     alignas(64) CUtensorMap tm_q;
     if (encode_tmap_2d(&tm_q, q, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(n_q),
-                       static_cast<uint64_t>(hidden) * 2, 64, BQ))
+                       static_cast<uint64_t>(hidden) * 2, 64, BQT))
         return KVQ_ERR_CUDA;
     AttnParams p{};
     p.n_q = n_q;
@@ -641,13 +687,10 @@ int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int h
     }
     p.tiles_before[ranges.n] = tiles;
     p.total_tiles = tiles;
-    // P reaches the second MMA through TMEM unless KVQ_ATTN_P_SMEM=1 selects shared memory
-    const char *env = getenv("KVQ_ATTN_P_SMEM");
-    const bool p_tmem = !(env && env[0] == '1');
     dim3 grid(static_cast<unsigned>((n_q + BQ - 1) / BQ), static_cast<unsigned>(hidden / 128));
-    if (group == 32) return launch_group<32>(tm_q, p, grid, mixed, p_tmem, s);
-    if (group == 64) return launch_group<64>(tm_q, p, grid, mixed, p_tmem, s);
-    return launch_group<128>(tm_q, p, grid, mixed, p_tmem, s);
+    if (group == 32) return launch_group<32>(tm_q, p, grid, mixed, s);
+    if (group == 64) return launch_group<64>(tm_q, p, grid, mixed, s);
+    return launch_group<128>(tm_q, p, grid, mixed, s);
 }
 
 cudaError_t read_clear_err_attn(unsigned int *v) {

@@ -38,18 +38,8 @@ def _assert_close(got, ref):
     return float(err.max()), float(rel)
 
 
-@pytest.fixture(params=["tmem", "smem"])
-def p_path(request, monkeypatch):
-    # P (the softmax weights) can reach the second MMA through TMEM or shared memory
-    if request.param == "smem":
-        monkeypatch.setenv("KVQ_ATTN_P_SMEM", "1")
-    else:
-        monkeypatch.delenv("KVQ_ATTN_P_SMEM", raising=False)
-    return request.param
-
-
-@pytest.mark.parametrize("n_q,n_kv,heads", [(77, 1, 2), (128, 128, 2), (300, 129, 2), (129, 1000, 3)])
-def test_random_store_fp32(p_path, n_q, n_kv, heads):
+@pytest.mark.parametrize("n_q,n_kv,heads", [(77, 1, 2), (128, 128, 2), (256, 256, 1), (300, 129, 2), (129, 1000, 3), (513, 2000, 2)])
+def test_random_store_fp32(n_q, n_kv, heads):
     st = _store(heads, n_kv, seed=n_kv)
     q = inputs.random_q(n_q, heads * 128, seed=n_q, std=2.0).cuda()
     out = kvq.packed_kv_attention(q, st, out_fp32=True)
