@@ -21,19 +21,25 @@
 //              the first 64 TMEM columns of its own S, and at the end divides
 //              by the row sum, un-rotates the row with the 128-point fast
 //              Walsh-Hadamard transform in registers and stores it.
-//   WG2        dequantisers: per 128-key tile, load the INT4 / INT8 codes and
-//              fp16 scales straight from global memory (issued one tile
-//              ahead), decode them with integer bit tricks into FP16
-//              (code * scale) and store K^ [key][dim] and V^T [dim][key] in
-//              the 128-byte-swizzled K-major layout the tensor core reads.
-//              K^'s dims are permuted inside each 8-dim chunk (the order
-//              e0 e4 e1 e5 e2 e6 e3 e7 falls out of the nibble decode); Q is
+//   WG2 + warps 14-15   dequantisers (192 threads): per 128-key tile, read
+//              the INT4 / INT8 codes from a shared-memory staging buffer and
+//              the fp16 scales from global memory (a tile ahead), decode them
+//              with integer bit tricks into FP16 (code * scale) and store K^
+//              and V^, both [key][dim], in the 128-byte-swizzled layout the
+//              tensor core reads (K^ as the K-major B operand of Q.K^T, V^ as
+//              the MN-major B operand of P.V^).  K^ is decoded as soon as the
+//              last Q.K^T of its stage has run, V^ once the last P.V^ has.
+//              The dims are permuted inside each 8-dim chunk (the order
+//              e0 e4 e1 e5 e2 e6 e3 e7 falls out of the nibble decode): Q is
 //              permuted the same way when it is converted, so Q.K^T is
-//              unchanged.  They also convert the BF16 Q tiles to FP16 once.
-//   WG3        warp 12: TMA of the Q tiles, TMEM allocation and the single
-//              MMA thread; warps 13-15 idle.
-// Registers are redistributed with setmaxnreg: 176 per softmax thread, 104
-// per dequantiser, 56 for WG3 (512 threads x 128 at launch).
+//              unchanged, and the output columns come out in the same order
+//              and are put back in the epilogue.  They also convert the BF16
+//              Q tiles to FP16 once.
+//   warp 12    TMA of the Q tiles, TMEM allocation and the single MMA thread.
+//   warp 13    bulk copies (TMA engine) of each tile's contiguous codes into
+//              the staging buffer, one tile ahead.
+// Registers are redistributed with setmaxnreg: 168 per softmax thread, 88
+// for the rest (512 threads x 128 at launch).
 // TMEM (512 columns): S_A, S_B, O_A, O_B, 128 columns each; P_t aliases the
 // first 64 columns of S_t.  tcgen05.mma instructions from one thread execute
 // in issue order, so S_t(j+1), issued after P_t(j).V^(j), overwrites P_t(j)
@@ -49,7 +55,6 @@
 #include <cuda_fp16.h>
 
 #include <cstdlib>
-#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -65,12 +70,12 @@ constexpr int NQT = 2;         // query tiles per CTA
 constexpr int BQ = BQT * NQT;  // query rows per CTA
 constexpr int BKV = 128;       // keys per tile
 constexpr int KV_STAGES = 2;   // K^ / V^T shared-memory stages
-constexpr int NUM_DQ_THREADS = 128;
-constexpr int NUM_SM_THREADS = 128;  // per query tile
+constexpr int NUM_DQ_THREADS = 192;   // warps 8-11 and 14-15
+constexpr int NUM_SM_THREADS = 128;   // per query tile
 constexpr int NUM_THREADS = 512;
-constexpr int WARP_MMA = 12;
-constexpr int REG_SOFTMAX = 176, REG_DEQUANT = 104, REG_MMA = 56;
-static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_DEQUANT + 128 * REG_MMA <= NUM_THREADS * 128,
+constexpr int WARP_MMA = 12, WARP_LOAD = 13;
+constexpr int REG_SOFTMAX = 168, REG_OTHER = 88;
+static_assert(2 * 128 * REG_SOFTMAX + 2 * 128 * REG_OTHER <= NUM_THREADS * 128,
               "register split exceeds the launch budget");
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128x128 fp16 operand tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;
@@ -90,12 +95,28 @@ struct AttnParams {
     int tiles_before[KVQ_MAX_RANGES + 1];
 };
 
+// Staging buffers of packed codes (as they sit in the store: 128 consecutive
+// key rows of one head), filled by bulk copies.  Two stages for INT4-only
+// stores, one (sized for INT8) when a store may hold INT8 ranges.
+template <bool MIXED>
+struct Staging {
+    static constexpr int CB = MIXED ? 128 : 64;  // code bytes per key row, largest case
+    static constexpr int STAGES = MIXED ? 1 : 2;
+    static constexpr int KC = 0;
+    static constexpr int VC = KC + 128 * CB;
+    static constexpr int STAGE_BYTES = VC + 128 * CB;
+    static constexpr int BYTES = STAGES * STAGE_BYTES;
+};
+
+// Dynamic shared memory, 1024-byte aligned (checked at run time): no slack.
+template <int GROUP, bool MIXED>
 struct SmemLayout {
     static constexpr int Q = 0;                           // NQT tiles
     static constexpr int K = Q + NQT * TILE_BYTES;        // KV_STAGES tiles
     static constexpr int V = K + KV_STAGES * TILE_BYTES;  // KV_STAGES tiles
-    static constexpr int BAR = V + KV_STAGES * TILE_BYTES;
-    static constexpr int BYTES = BAR + 256 + 1024;
+    static constexpr int STG = V + KV_STAGES * TILE_BYTES;
+    static constexpr int BAR = STG + Staging<MIXED>::BYTES;
+    static constexpr int BYTES = BAR + 256;
 };
 
 // Physical byte offset of 16-byte chunk `c` (0..15 along K) of row `r` in a
@@ -155,9 +176,6 @@ __device__ __forceinline__ uint32_t dq_int8_pair(uint32_t a, uint32_t b, uint32_
     return h2_mul(h2_add(t, H2_NEG1152), s2);
 }
 __device__ __forceinline__ uint32_t h2_dup(uint16_t s) { return static_cast<uint32_t>(s) * 0x10001u; }
-__device__ __forceinline__ uint32_t h2_pack(uint16_t lo, uint16_t hi) {
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
 __device__ __forceinline__ uint64_t f2_pack(float a, float b) {
@@ -216,130 +234,74 @@ __device__ __forceinline__ TileRef tile_ref(const AttnParams &p, int j) {
     return t;
 }
 
-// Raw codes a dequantiser thread holds for one tile (MIXED = INT8 possible).
+// A tile's decode work is split into units of 16 staged code bytes: unit u of
+// the tile's 2 x 128 x (code bytes per row / 16) units is K (first half) or
+// V (second half), key row rem / cpr, 16-byte column rem % cpr (cpr = 4 for
+// INT4, 8 for INT8).  Dequantiser d takes units d, d + 192, d + 384, ...; a
+// warp's 32 consecutive units are 512 contiguous staged bytes.
 template <bool MIXED>
-struct RawTile {
-    uint4 k[MIXED ? 8 : 4];                                     // one key row: 64 (INT4) or 128 (INT8) bytes
-    typename std::conditional<MIXED, uint4, uint2>::type v[8];  // 8 keys x 16 dims (8 B INT4, 16 B INT8)
-    uint16_t ks[4];                                             // scales of the key row (128/GROUP used)
-    uint16_t vs[8];                                             // scale of each of the 8 keys, 16-dim block
-    int bits;
+struct UnitPlan {
+    static constexpr int MAX_UNITS = MIXED ? 11 : 6;  // ceil(2*128*cpr / 192)
 };
 
+// fp16 scale of each unit of dequantiser d for tile j (0 for rows past the
+// tile's valid keys), loaded straight from global memory one tile ahead: a
+// warp's loads cover contiguous bytes.
 template <int GROUP, bool MIXED>
-__device__ __forceinline__ void load_raw(const AttnParams &p, int head, int j, int tid, RawTile<MIXED> &R) {
+__device__ __forceinline__ void load_scales(const AttnParams &p, int head, int j, int d,
+                                            uint32_t (&sc)[UnitPlan<MIXED>::MAX_UNITS]) {
+    constexpr int SG = 128 / GROUP;
     const TileRef t = tile_ref(p, j);
     const RangeDev &rg = p.ranges.r[t.g];
-    const int bits = MIXED ? rg.bits : 4;
-    R.bits = bits;
-    const int cb = bits == 4 ? 64 : 128;
-    constexpr int SG = 128 / GROUP;
-    {  // K unit: key row tid
-        const int r = tid;
-        if (r < t.valid) {
-            const int64_t row = static_cast<int64_t>(head) * rg.cap + t.key0 + r;
-            const uint4 *src = reinterpret_cast<const uint4 *>(rg.k_codes + row * cb);
+    const int64_t row0 = static_cast<int64_t>(head) * rg.cap + t.key0;
+    const int cpr = (MIXED && rg.bits == 8) ? 8 : 4;
+    const int uh = 128 * cpr;
 #pragma unroll
-            for (int i = 0; i < (MIXED ? 8 : 4); ++i)
-                if (i < cb / 16) R.k[i] = ld_global_nc_v4(src + i);
-            const uint16_t *ss = rg.k_scales + row * SG;
-#pragma unroll
-            for (int g = 0; g < SG; ++g) R.ks[g] = __ldg(ss + g);
-        } else {
-#pragma unroll
-            for (int i = 0; i < (MIXED ? 8 : 4); ++i) R.k[i] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int g = 0; g < SG; ++g) R.ks[g] = 0;
-        }
-    }
-    {  // V unit: keys 8*kb .. 8*kb+7, dims 16*db .. 16*db+15
-        const int kb = tid & 15, db = tid >> 4;
-        const int g = (16 * db) / GROUP;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int r = 8 * kb + k;
-            if (r < t.valid) {
-                const int64_t row = static_cast<int64_t>(head) * rg.cap + t.key0 + r;
-                if constexpr (MIXED) {
-                    if (bits == 4) {
-                        const uint2 x = *reinterpret_cast<const uint2 *>(rg.v_codes + row * 64 + db * 8);
-                        R.v[k] = make_uint4(x.x, x.y, 0, 0);
-                    } else {
-                        R.v[k] = ld_global_nc_v4(rg.v_codes + row * 128 + db * 16);
-                    }
-                } else {
-                    R.v[k] = *reinterpret_cast<const uint2 *>(rg.v_codes + row * 64 + db * 8);
-                }
-                R.vs[k] = __ldg(rg.v_scales + row * SG + g);
-            } else {
-                R.v[k] = {};
-                R.vs[k] = 0;
-            }
-        }
+    for (int i = 0; i < UnitPlan<MIXED>::MAX_UNITS; ++i) {
+        const int u = d + NUM_DQ_THREADS * i;
+        const int kv = u >= uh ? 1 : 0;
+        const int rem = u - kv * uh;
+        const int r = rem / cpr;
+        const int g = ((rem % cpr) * (128 / cpr)) / GROUP;
+        const uint16_t *base = kv ? rg.v_scales : rg.k_scales;
+        sc[i] = (u < 2 * uh && r < t.valid) ? static_cast<uint32_t>(__ldg(base + (row0 + r) * SG + g)) : 0u;
     }
 }
 
-template <int GROUP, bool MIXED>
-__device__ __forceinline__ void store_tile(const RawTile<MIXED> &R, uint8_t *k_tile, uint8_t *v_tile, int tid) {
-    {  // K^ row tid: 16 chunks of 8 dims (permuted e0 e4 e1 e5 e2 e6 e3 e7)
-        const int r = tid;
+// Decodes unit u of a staged tile into K^ or V^ ([key][dim], 128-byte
+// swizzle, dims permuted inside each 8-dim chunk); rows past `valid` become zeros.
+template <bool MIXED>
+__device__ __forceinline__ void decode_unit(const uint8_t *stg, int u, int bits, int valid, uint32_t scale,
+                                            uint8_t *k_tile, uint8_t *v_tile) {
+    using SL = Staging<MIXED>;
+    const int cpr = (MIXED && bits == 8) ? 8 : 4;
+    const int uh = 128 * cpr;
+    const int kv = u >= uh ? 1 : 0;
+    const int rem = u - kv * uh;
+    const int r = rem / cpr, cc = rem % cpr;
+    const uint4 w = *reinterpret_cast<const uint4 *>(stg + (kv ? SL::VC : SL::KC) + r * (16 * cpr) + cc * 16);
+    uint8_t *tile = kv ? v_tile : k_tile;
+    const bool live = r < valid;
+    const uint32_t s2 = h2_dup(static_cast<uint16_t>(scale));
+    if (!MIXED || bits == 4) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint32_t s2 = h2_dup(R.ks[(c * 8) / GROUP]);
-            uint32_t o[4];
-            if (!MIXED || R.bits == 4) {
-                const uint32_t w = (&R.k[c >> 2].x)[c & 3];
-                dq_int4_word(w, s2, o);
-            } else {
-                const uint32_t a = (&R.k[c >> 1].x)[(c & 1) * 2];
-                const uint32_t b = (&R.k[c >> 1].x)[(c & 1) * 2 + 1];
+        for (int k = 0; k < 4; ++k) {  // dims 32cc + 8k .. +7
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            if (live) dq_int4_word((&w.x)[k], s2, o);
+            *reinterpret_cast<uint4 *>(tile + sw128_off(r, 4 * cc + k)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // dims 16cc + 8k .. +7
+            const uint32_t a = (&w.x)[2 * k], b = (&w.x)[2 * k + 1];
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            if (live) {
                 o[0] = dq_int8_pair(a, b, 0x0400u, s2);
                 o[1] = dq_int8_pair(a, b, 0x0501u, s2);
                 o[2] = dq_int8_pair(a, b, 0x0602u, s2);
                 o[3] = dq_int8_pair(a, b, 0x0703u, s2);
             }
-            *reinterpret_cast<uint4 *>(k_tile + sw128_off(r, c)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    }
-    {  // V^T rows 16*db .. 16*db+15, chunk kb (keys 8kb .. 8kb+7, natural order)
-        const int kb = tid & 15, db = tid >> 4;
-        uint32_t s2[4];
-#pragma unroll
-        for (int kp = 0; kp < 4; ++kp) s2[kp] = h2_pack(R.vs[2 * kp], R.vs[2 * kp + 1]);
-        if (!MIXED || R.bits == 4) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {  // dims 4q .. 4q+3 of the 16-dim block
-                uint32_t out[4][4];         // [dim][key pair]
-#pragma unroll
-                for (int kp = 0; kp < 4; ++kp) {
-                    const uint32_t aw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp])[q >> 1];
-                    const uint32_t bw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp + 1])[q >> 1];
-                    // low half: 4 dims of key a, high half: the same 4 dims of key a+1
-                    const uint32_t x = prmt(aw, bw, (q & 1) ? 0x7632u : 0x5410u);
-                    uint32_t o[4];
-                    dq_int4_word(x, s2[kp], o);
-#pragma unroll
-                    for (int d = 0; d < 4; ++d) out[d][kp] = o[d];
-                }
-#pragma unroll
-                for (int d = 0; d < 4; ++d)
-                    *reinterpret_cast<uint4 *>(v_tile + sw128_off(16 * db + 4 * q + d, kb)) =
-                        make_uint4(out[d][0], out[d][1], out[d][2], out[d][3]);
-            }
-        } else {
-#pragma unroll
-            for (int d = 0; d < 16; ++d) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int kp = 0; kp < 4; ++kp) {
-                    const uint32_t aw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp])[d >> 2];
-                    const uint32_t bw = reinterpret_cast<const uint32_t *>(&R.v[2 * kp + 1])[d >> 2];
-                    const uint32_t bi = static_cast<uint32_t>(d & 3);
-                    w4[kp] = dq_int8_pair(aw, bw, bi | ((4u + bi) << 8), s2[kp]);
-                }
-                *reinterpret_cast<uint4 *>(v_tile + sw128_off(16 * db + d, kb)) =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+            *reinterpret_cast<uint4 *>(tile + sw128_off(r, 2 * cc + k)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
 }
@@ -355,21 +317,29 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 template <int GROUP, bool MIXED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttnParams p) {
-    using L = SmemLayout;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = SmemLayout<GROUP, MIXED>;
+    using SL = Staging<MIXED>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (smem_u32(smem) & 1023u) {  // the layout below assumes a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicOr(&g_err_attn, 2u);
+        return;
+    }
     uint8_t *sQ = smem + L::Q;
     uint8_t *sK = smem + L::K;
     uint8_t *sV = smem + L::V;
+    uint8_t *sStg = smem + L::STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
     uint64_t *q_tma = bars + 0;
     uint64_t *q_ready = bars + 1;
     uint64_t *kv_full = bars + 2;   // [KV_STAGES]
-    uint64_t *kv_empty = bars + 4;  // [KV_STAGES]
+    uint64_t *k_empty = bars + 4;   // [KV_STAGES]: K^ stage read by its last Q.K^T
     uint64_t *s_full = bars + 6;    // [NQT]
     uint64_t *p_full = bars + 8;    // [NQT]
     uint64_t *pv_done = bars + 10;  // [NQT]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *stg_full = bars + 12;   // [SL::STAGES]
+    uint64_t *stg_empty = bars + 14;  // [SL::STAGES]
+    uint64_t *v_empty = bars + 16;    // [KV_STAGES]: V^ stage read by its last P.V^
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -382,12 +352,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(q_ready, NUM_DQ_THREADS);
         for (int i = 0; i < KV_STAGES; ++i) {
             mbar_init(&kv_full[i], NUM_DQ_THREADS);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < NQT; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], NUM_SM_THREADS);
             mbar_init(&pv_done[i], 1);
+        }
+        for (int i = 0; i < SL::STAGES; ++i) {
+            mbar_init(&stg_full[i], 1);
+            mbar_init(&stg_empty[i], NUM_DQ_THREADS);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -401,9 +376,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp >= 12) {
-        setmaxnreg_dec<REG_MMA>();
-        // ------------------------------------------------------------ WG3: Q load + MMA issue
+    if (warp >= 8) {
+    setmaxnreg_dec<REG_OTHER>();  // WG2 and WG3, one instruction for both warpgroups
+    if (warp >= 12 && warp < 14) {
+        // ------------------------------------------------------------ warp 12: Q load + MMA issue
         if (warp == WARP_MMA) {
             if (elect_one()) {
                 prefetch_tmap(&tm_q);
@@ -415,6 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tma_load_2d(sQ + t * TILE_BYTES + HALF_BYTES, &tm_q, q_tma, head * 128 + 64, y);
                 }
                 constexpr uint32_t idesc = make_idesc_f16(128, 128, 0);
+                constexpr uint32_t idesc_pv = make_idesc_f16(128, 128, 0, 1);  // V^ [key][dim]: MN-major B
                 const uint32_t qa = smem_u32(sQ);
                 bool ok = mbar_wait(q_ready, 0, abort_flag, &g_err_attn);
                 tc_fence_after();
@@ -435,6 +412,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tc_fence_after();
                         issue_s(0, 0);
                         issue_s(0, 1);
+                        mma_commit(&k_empty[0]);
                     }
                 }
                 for (int j = 0; ok && j < T; ++j) {
@@ -446,13 +424,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                            mma_f16_ts(tmem + tm_o(t), tmem + tm_s(t) + k * 8, make_sdesc_sw128(vb + off), idesc,
+                        for (int k = 0; k < 8; ++k) {  // keys 16k .. 16k+15: 16 rows of V^
+                            mma_f16_ts(tmem + tm_o(t), tmem + tm_s(t) + k * 8,
+                                       make_sdesc_sw128_mn(vb + k * 2048, HALF_BYTES), idesc_pv,
                                        (j > 0 || k > 0) ? 1u : 0u);
                         }
                         mma_commit(&pv_done[t]);
-                        if (t == NQT - 1) mma_commit(&kv_empty[st]);
+                        if (t == NQT - 1) mma_commit(&v_empty[st]);
                         if (j + 1 < T) {
                             if (t == 0) {
                                 ok = mbar_wait(&kv_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, abort_flag,
@@ -461,6 +439,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 tc_fence_after();
                             }
                             issue_s(j + 1, t);
+                            if (t == NQT - 1) mma_commit(&k_empty[(j + 1) % KV_STAGES]);
                         }
                     }
                 }
@@ -473,16 +452,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mbar_wait(q_tma, 0, &no_abort, nullptr);
             }
             __syncwarp();
+        } else {
+            // ------------------------------------------------------------ bulk copies of the codes
+            if (elect_one()) {
+                uint32_t armed = 0, armed_parity = 0;
+                for (int j = 0; j < T && !*abort_flag; ++j) {
+                    const int s = j % SL::STAGES;
+                    if (!mbar_wait(&stg_empty[s], ((j / SL::STAGES) & 1) ^ 1, abort_flag, &g_err_attn)) break;
+                    const TileRef tr = tile_ref(p, j);
+                    const RangeDev &rg = p.ranges.r[tr.g];
+                    const uint32_t cb = (MIXED && rg.bits == 8) ? 128u : 64u;
+                    const int64_t row0 = static_cast<int64_t>(head) * rg.cap + tr.key0;
+                    uint8_t *dst = sStg + s * SL::STAGE_BYTES;
+                    mbar_arrive_expect_tx(&stg_full[s], 2u * 128u * cb);
+                    bulk_load(dst + SL::KC, rg.k_codes + row0 * cb, 128u * cb, &stg_full[s]);
+                    bulk_load(dst + SL::VC, rg.v_codes + row0 * cb, 128u * cb, &stg_full[s]);
+                    armed |= 1u << s;
+                    armed_parity = (armed_parity & ~(1u << s)) | (static_cast<uint32_t>((j / SL::STAGES) & 1) << s);
+                }
+                // drain: the last copies have landed before the CTA exits
+                volatile int no_abort = 0;
+                for (int s = 0; s < SL::STAGES; ++s)
+                    if (armed & (1u << s)) mbar_wait(&stg_full[s], (armed_parity >> s) & 1u, &no_abort, nullptr);
+            }
+            __syncwarp();
         }
-    } else if (warp >= 8) {
-        setmaxnreg_dec<REG_DEQUANT>();
-        // ------------------------------------------------------------ WG2: dequantisers
-        const int tid = threadIdx.x - 256;  // 0..127
+    } else {
+        // ------------------------------------------------------------ dequantisers (warps 8-11, 14-15)
+        const int d = warp < 12 ? static_cast<int>(threadIdx.x) - 256 : static_cast<int>(threadIdx.x) - 448 + 128;
         // Q: BF16 -> FP16 in place, dims permuted e0 e4 e1 e5 e2 e6 e3 e7 within each 8-chunk
         const bool ok = mbar_wait(q_tma, 0, abort_flag, &g_err_attn);
         if (ok) {
-#pragma unroll 4
-            for (int i = tid; i < NQT * TILE_BYTES / 16; i += NUM_DQ_THREADS) {
+#pragma unroll 2
+            for (int i = d; i < NQT * TILE_BYTES / 16; i += NUM_DQ_THREADS) {
                 uint4 *c = reinterpret_cast<uint4 *>(sQ + i * 16);
                 const uint4 v = *c;
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -503,16 +505,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
         }
         mbar_arrive(q_ready);
-        RawTile<MIXED> raw;
-        if (ok && T > 0) load_raw<GROUP, MIXED>(p, head, 0, tid, raw);
+        uint32_t sc[UnitPlan<MIXED>::MAX_UNITS];
+        if (ok && T > 0) load_scales<GROUP, MIXED>(p, head, 0, d, sc);
         for (int j = 0; ok && j < T && !*abort_flag; ++j) {
             const int st = j % KV_STAGES;
-            if (!mbar_wait(&kv_empty[st], ((j / KV_STAGES) & 1) ^ 1, abort_flag, &g_err_attn)) break;
-            store_tile<GROUP, MIXED>(raw, sK + st * TILE_BYTES, sV + st * TILE_BYTES, tid);
+            const int s = j % SL::STAGES;
+            const uint32_t ph = ((j / KV_STAGES) & 1) ^ 1;
+            if (!mbar_wait(&stg_full[s], (j / SL::STAGES) & 1, abort_flag, &g_err_attn)) break;
+            const TileRef tr = tile_ref(p, j);
+            const int bits = MIXED ? p.ranges.r[tr.g].bits : 4;
+            const int uh = 128 * ((MIXED && bits == 8) ? 8 : 4);
+            const uint8_t *stg = sStg + s * SL::STAGE_BYTES;
+            uint8_t *kt = sK + st * TILE_BYTES;
+            uint8_t *vt = sV + st * TILE_BYTES;
+            bool fine = mbar_wait(&k_empty[st], ph, abort_flag, &g_err_attn);
+            bool v_free = false;
+#pragma unroll
+            for (int i = 0; i < UnitPlan<MIXED>::MAX_UNITS && fine; ++i) {
+                const int u = d + NUM_DQ_THREADS * i;
+                if (u >= 2 * uh) break;
+                if (u >= uh && !v_free) {
+                    fine = mbar_wait(&v_empty[st], ph, abort_flag, &g_err_attn);
+                    v_free = true;
+                    if (!fine) break;
+                }
+                decode_unit<MIXED>(stg, u, bits, tr.valid, sc[i], kt, vt);
+            }
+            if (fine && !v_free) fine = mbar_wait(&v_empty[st], ph, abort_flag, &g_err_attn);
+            if (!fine) break;
+            mbar_arrive(&stg_empty[s]);  // every staged byte of this tile has been read
             fence_proxy_async_smem();
             mbar_arrive(&kv_full[st]);
-            if (j + 1 < T) load_raw<GROUP, MIXED>(p, head, j + 1, tid, raw);
+            if (j + 1 < T) load_scales<GROUP, MIXED>(p, head, j + 1, d, sc);
         }
+    }
     } else {
         setmaxnreg_inc<REG_SOFTMAX>();
         // ------------------------------------------------------------ WG0 / WG1: softmax + epilogue
@@ -572,14 +598,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float x0, x1, x2, x3;
                 f2_unpack(a0, x0, x1);
                 f2_unpack(a1, x2, x3);
-                const __half2 h0 = __floats2half2_rn(ex2_approx(x0), ex2_approx(x1));
-                const __half2 h1 = __floats2half2_rn(ex2_approx(x2), ex2_approx(x3));
+                x0 = ex2_approx(x0);
+                x1 = ex2_approx(x1);
+                x2 = ex2_approx(x2);
+                x3 = ex2_approx(x3);
+                const __half2 h0 = __floats2half2_rn(x0, x1);
+                const __half2 h1 = __floats2half2_rn(x2, x3);
                 pk[c >> 1] = *reinterpret_cast<const uint32_t *>(&h0);
                 pk[(c >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h1);
-                // the row sum uses the same FP16-rounded weights the MMA sees
-                const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-                acc0 = f2_add(acc0, f2_pack(f0.x, f0.y));
-                acc1 = f2_add(acc1, f2_pack(f1.x, f1.y));
+                // the row sum takes the fp32 weights (the MMA sees them rounded to FP16,
+                // a relative 2^-12 per weight that averages out in the sum)
+                acc0 = f2_add(acc0, f2_pack(x0, x1));
+                acc1 = f2_add(acc1, f2_pack(x2, x3));
             }
             float u0, u1, u2, u3;
             f2_unpack(acc0, u0, u1);
@@ -610,9 +640,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t oraw[128];
             tmem_ld128(oa, oraw);
             const float inv_l = 1.0f / l;
+            // V^'s dims, hence O's columns, are in the order e0 e4 e1 e5 e2 e6 e3 e7 per 8-dim chunk
             float o[128];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) o[c] = __uint_as_float(oraw[c]) * inv_l;
+            for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    o[c + e] = __uint_as_float(oraw[c + 2 * e]) * inv_l;
+                    o[c + 4 + e] = __uint_as_float(oraw[c + 2 * e + 1]) * inv_l;
+                }
+            }
             rotate128_thread(o);
             const int64_t row = q0 + t * BQT + r;
             if (row < p.n_q) {
@@ -648,7 +685,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <int GROUP, bool MIXED>
 int launch_one(const CUtensorMap &tm, const AttnParams &p, dim3 grid, cudaStream_t s) {
-    constexpr int smem = SmemLayout::BYTES;
+    constexpr int smem = SmemLayout<GROUP, MIXED>::BYTES;
     auto fn = attention_kernel<GROUP, MIXED>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) {

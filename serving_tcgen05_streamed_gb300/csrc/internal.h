@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/kvq.h"
+#include "kvq.h"
 
 namespace kvq {
 

@@ -167,14 +167,16 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// Instruction descriptor for kind::f16: FP32 accumulator, A/B both K-major.
-// ab_bf16: 1 = BF16 operands, 0 = FP16 operands.
-__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, int ab_bf16) {
-    return (1u << 4)                                   // D format: F32
-           | (static_cast<uint32_t>(ab_bf16) << 7)     // A format
-           | (static_cast<uint32_t>(ab_bf16) << 10)    // B format
-           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
-           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+// Instruction descriptor for kind::f16: FP32 accumulator, A K-major, B K-major
+// (b_mn_major = 0) or MN-major (b_mn_major = 1).  ab_bf16: 1 = BF16 operands,
+// 0 = FP16 operands.
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, int ab_bf16, int b_mn_major = 0) {
+    return (1u << 4)                                    // D format: F32
+           | (static_cast<uint32_t>(ab_bf16) << 7)      // A format
+           | (static_cast<uint32_t>(ab_bf16) << 10)     // B format
+           | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }
 
 // Shared-memory matrix descriptor for a K-major operand in the 128-byte
@@ -188,6 +190,22 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t smem_addr) {
     d |= static_cast<uint64_t>(1024u >> 4) << 32;                // stride byte offset: 8 rows x 128 B
     d |= static_cast<uint64_t>(1u) << 46;                        // descriptor version (sm_100 family)
     d |= static_cast<uint64_t>(2u) << 61;                        // layout: 128-byte swizzle
+    return d;
+}
+
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzle layout: each 128-byte row holds 64 consecutive MN elements of one K
+// index, 8 rows (K indices) form a 1024-byte atom; `mn_atom_stride` bytes
+// separate atoms along MN (leading byte offset), 1024 bytes separate 8-row
+// groups along K (stride byte offset).  A K-step of 16 advances the start by
+// two atoms' rows (2048 bytes).
+__device__ __forceinline__ uint64_t make_sdesc_sw128_mn(uint32_t smem_addr, uint32_t mn_atom_stride) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_atom_stride >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
     return d;
 }
 
