@@ -243,16 +243,34 @@ def run_gpu(args, wl, world, rank, local):
         x = x.roll(rank * 7, dims=0)
     fp, fa = flops(n, C)
 
-    peak_ours, peak_mat = peak_memory(wl, x, w, qn, kn, kvq)
-
+    mixed = wl is inputs.MIXED
+    if mixed:  # INT8 for the conditioning ranges, rotated INT4 for the generated video
+        stores = [kvq.PackedKV.empty(seg_n, C, 32, bits, dev) for _, seg_n, bits in inputs.MIXED_SEGMENTS]
+        peak_ours = peak_mat = None
+    else:
+        peak_ours, peak_mat = peak_memory(wl, x, w, qn, kn, kvq)
+        stores = [kvq.PackedKV.empty(n, C, 32, 4, dev)]
+    store = stores[0]
     q = torch.empty((n, C), dtype=torch.bfloat16, device=dev)
-    store = kvq.PackedKV.empty(n, C, 32, 4, dev)
+
+    def project(xin):
+        if mixed:
+            kvq.streamed_qkv_proj_mixed(xin, w, stores, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
+                                        k_norm_w=kn, q_out=q, stream=stream)
+        else:
+            kvq.streamed_qkv_proj(xin, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q,
+                                  store=store, stream=stream)
+
+    def attend():
+        if mixed:
+            kvq.packed_kv_attention_mixed(q, stores, out=q, stream=stream)
+        else:
+            kvq.packed_kv_attention(q, store, out=q, stream=stream)
 
     def step():
-        kvq.streamed_qkv_proj(x, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q,
-                              store=store, stream=stream)
+        project(x)
         ev_a0.record(stream)
-        kvq.packed_kv_attention(q, store, out=q, stream=stream)
+        attend()
         ev_a1.record(stream)
 
     ev_a0, ev_a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -296,9 +314,8 @@ def run_gpu(args, wl, world, rank, local):
             barrier(world)
             t0 = time.perf_counter()
         x_dev.copy_(x_host, non_blocking=True)
-        kvq.streamed_qkv_proj(x_dev, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q,
-                              store=store, stream=stream)
-        kvq.packed_kv_attention(q, store, out=q, stream=stream)
+        project(x_dev)
+        attend()
         out_host.copy_(q, non_blocking=True)
         torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
@@ -322,7 +339,7 @@ def run_gpu(args, wl, world, rank, local):
                 traffic = rec.get("bytes_per_launch")
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not mixed:
         del x_host, out_host, x_dev
         sample = CpuOracleSample(wl, seed=7, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
         t_block = sample.run()
@@ -336,9 +353,10 @@ def run_gpu(args, wl, world, rank, local):
             "vs_baseline": None, "dtype": "bf16 GEMM / fp16 attention operands, fp32 accumulate",
             "data": "synthetic (seeded generators; random-init weights of the H3 block shape)",
             "config": {"workload": wl.name, "n_tokens": n, "hidden": C, "heads": wl.heads, "group": 32,
-                       "kv_bits": 4, "chunk_tokens": wl.chunk_tokens, "qk_rmsnorm": True,
+                       "kv_bits": "8/4 by token range" if mixed else 4, "chunk_tokens": wl.chunk_tokens,
+                       "qk_rmsnorm": True,
                        "l2": f"inputs larger than L2 (x {n * C * 2 / GiB:.2f} GiB, packed K/V "
-                             f"{store.nbytes() / GiB:.2f} GiB)",
+                             f"{sum(st.nbytes() for st in stores) / GiB:.2f} GiB)",
                        "parallelism": f"independent blocks x{world}"},
             "tokens_per_s": world * n / (ms_per_step * 1e-3),
             "kernel_ms": {"qkv_proj": ms_per_step - attn_avg_ms, "attention": attn_avg_ms},
@@ -346,6 +364,7 @@ def run_gpu(args, wl, world, rank, local):
                               "attention": attn_tflops},
             "peak_gib": peak_ours, "peak_gib_materialise_bf16_qkv": peak_mat,
             "peak_ratio": peak_ours / peak_mat if peak_mat else None,
+            "kv_store": [{"tokens": st.n, "bits": st.bits} for st in stores],
             "roofline": {"kernel": "packed_kv_attention", "bound": "tensor", "achieved": attn_tflops,
                          "peak": peak, "unit": "TFLOP/s", "frac": attn_tflops / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} bf16 sustained (fp16 dense rate = bf16 dense rate)"},
@@ -360,6 +379,60 @@ def run_gpu(args, wl, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Bandwidth of the standalone rotate + quantise + pack kernel and of its
+    inverse over the sweep sizes (K/V BF16 [N, 2 x 7168], groups 32/64/128),
+    against the measured HBM copy bandwidth.  L2 is flushed (a 512 MiB write)
+    before every timed launch."""
+    import serving_tcgen05_streamed_gb300 as kvq
+    from serving_tcgen05_streamed_gb300 import inputs
+    kvq.load()
+    torch.cuda.set_device(0)
+    C = 7168
+    peaks, kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    rows = []
+    for n in inputs.SWEEP_N:
+        kv = inputs.sweep_kv(n, C, seed=0, device="cuda")
+        for g in inputs.SWEEP_GROUPS:
+            store = kvq.PackedKV.empty(n, C, g, 4, "cuda")
+            out = torch.empty_like(kv)
+            res = {}
+            for name, fn in (("pack", lambda: kvq.kv_rotate_quant_pack(kv, C, g, 4, out=store)),
+                             ("unpack", lambda: kvq.kv_unpack(store, C, out=out))):
+                ts = []
+                for i in range(args.warmup + args.steps):
+                    flush.fill_(i & 0xFF)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn()
+                    b.record()
+                    b.synchronize()
+                    if i >= args.warmup:
+                        ts.append(a.elapsed_time(b))
+                ms = statistics.median(ts)
+                nbytes = n * (2 * C * 2 + 2 * (C // 2 + (C // g) * 2))  # BF16 K/V + INT4 codes + fp16 scales
+                res[name] = {"ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9}
+            rows.append({"n": n, "group": g, "bytes": nbytes, "pack_ms": res["pack"]["ms"],
+                         "pack_gbs": res["pack"]["gbs"], "unpack_ms": res["unpack"]["ms"],
+                         "unpack_gbs": res["unpack"]["gbs"]})
+            del store, out
+        del kv
+    assert kvq.device_status() == kvq.KVQ_OK
+    best = max(rows, key=lambda r: r["pack_gbs"])
+    big = [r for r in rows if r["n"] == max(inputs.SWEEP_N) and r["group"] == 32][0]
+    print(json.dumps({
+        "metric": "kv_rotate_quant_pack bandwidth (BF16 K/V -> rotated INT4 + fp16 scales)", "value": big["pack_gbs"],
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "dtype": "bf16 in, int4 + fp16 out", "data": "synthetic: N(0,1) with 1% Student-t (nu=3) channels",
+        "config": {"workload": "K/V [N, 2x7168] sweep", "l2": "flushed before every launch"},
+        "roofline": {"kernel": "kv_rotate_quant_pack", "bound": "hbm", "achieved": big["pack_gbs"], "peak": hbm,
+                     "unit": "GB/s", "frac": big["pack_gbs"] / hbm, "peak_source": f"{kind} hbm copy",
+                     "at": {"n": big["n"], "group": 32}},
+        "best": best, "sweep": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -369,13 +442,17 @@ def main():
     ap.add_argument("--ref-proj-rows", type=int, default=16)
     ap.add_argument("--ref-attn-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("h3_ref2va", "mid"), default="h3_ref2va",
-                    help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling)")
+    ap.add_argument("--workload", choices=("h3_ref2va", "mid", "mixed", "sweep"), default="h3_ref2va",
+                    help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling); "
+                         "mixed: N=217,088 with INT8 conditioning ranges; sweep: pack/unpack bandwidth")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from serving_tcgen05_streamed_gb300 import inputs
-    wl = inputs.H3_REF2VA if args.workload == "h3_ref2va" else inputs.MID
+    if args.workload == "sweep":
+        run_sweep(args)
+        return
+    wl = {"h3_ref2va": inputs.H3_REF2VA, "mid": inputs.MID, "mixed": inputs.MIXED}[args.workload]
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, wl, int(os.environ.get("WORLD_SIZE", "1")), rank)

@@ -7,10 +7,13 @@
 // implemented in quant.cuh.
 //
 // Both kernels are HBM-bound: per token they move 2*hidden*2 bytes of BF16
-// and 2*hidden*(bits/8 + 2/group) bytes of codes and scales.  One warp owns
-// one 128-wide head vector (4 consecutive elements per lane); a block of 8
-// warps covers 8 head slots x 32 tokens, loading 8 tokens per warp before
-// computing so that enough bytes are in flight.
+// and 2*hidden*(bits/8 + 2/group) bytes of codes and scales.  Four lanes own
+// one 128-wide head vector, 32 consecutive elements each, so five of the seven
+// butterfly stages and (for groups of 32) the whole group absmax stay inside
+// a lane, and a lane's codes leave in one 16-byte store.  A warp works on 8
+// tokens of one head slot at a time (K heads, then V heads), two such passes
+// loaded ahead of the arithmetic; a block of 8 warps covers 8 head slots x 32
+// tokens.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -25,13 +28,7 @@ __device__ unsigned int g_err_quant;
 
 constexpr int kWarps = 8;
 constexpr int kTokensPerBlock = 32;
-constexpr int kBatch = 8;
-
-__device__ __forceinline__ uint2 ld_nc_u2(const void *p) {
-    uint2 v;
-    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
+constexpr int kPass = 8;  // tokens per warp pass (4 lanes per token)
 
 template <int GROUP, int BITS>
 __global__ void __launch_bounds__(kWarps * 32) rotate_quant_pack_kernel(const __nv_bfloat16 *__restrict__ kv,
@@ -42,44 +39,48 @@ __global__ void __launch_bounds__(kWarps * 32) rotate_quant_pack_kernel(const __
                                                                          uint16_t *__restrict__ v_scales) {
     constexpr int CB = 128 * BITS / 8;  // code bytes per head row
     constexpr int SG = 128 / GROUP;     // scales per head row
-    constexpr int LANES_PER_GROUP = GROUP / 4;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hs = blockIdx.y * kWarps + warp;  // head slot: K heads then V heads
     if (hs >= 2 * heads) return;
     const int kvi = hs >= heads ? 1 : 0;
     const int h = hs - kvi * heads;
+    const int q = lane & 3;
     uint8_t *codes = (kvi ? v_codes : k_codes) + static_cast<int64_t>(h) * cap * CB;
     uint16_t *scales = (kvi ? v_scales : k_scales) + static_cast<int64_t>(h) * cap * SG;
-    const __nv_bfloat16 *src = kv + static_cast<int64_t>(hs) * 128 + lane * 4;
-    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock;
+    const __nv_bfloat16 *src = kv + static_cast<int64_t>(hs) * 128 + q * 32;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock + (lane >> 2);
 
 #pragma unroll 1
-    for (int tb = 0; tb < kTokensPerBlock; tb += kBatch) {
-        uint2 raw[kBatch];
+    for (int p = 0; p < kTokensPerBlock / kPass; p += 2) {
+        uint4 raw[2][4];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int64_t t = t0 + tb + u;
-            raw[u] = (t < n) ? ld_nc_u2(src + t * ld) : make_uint2(0u, 0u);
+        for (int u = 0; u < 2; ++u) {
+            const int64_t t = t0 + (p + u) * kPass;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                raw[u][i] = (t < n) ? ld_global_nc_v4(src + t * ld + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int64_t t = t0 + tb + u;
-            float v[4];
-            v[0] = __uint_as_float(raw[u].x << 16);
-            v[1] = __uint_as_float(raw[u].x & 0xFFFF0000u);
-            v[2] = __uint_as_float(raw[u].y << 16);
-            v[3] = __uint_as_float(raw[u].y & 0xFFFF0000u);
-            rotate128_warp(v, lane);
-            uint16_t sbits;
-            const uint32_t packed = quant128_warp<GROUP, BITS>(v, sbits);
-            if (t < cap) {
-                if constexpr (BITS == 4) {
-                    reinterpret_cast<uint16_t *>(codes + t * CB)[lane] = static_cast<uint16_t>(packed);
-                } else {
-                    reinterpret_cast<uint32_t *>(codes + t * CB)[lane] = packed;
+        for (int u = 0; u < 2; ++u) {
+            const int64_t t = t0 + (p + u) * kPass;
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t w[4] = {raw[u][i].x, raw[u][i].y, raw[u][i].z, raw[u][i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
+                    v[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
                 }
-                if ((lane % LANES_PER_GROUP) == 0) scales[t * SG + lane / LANES_PER_GROUP] = sbits;
             }
+            rotate128_quad(v, lane);
+            uint32_t words[BITS];
+            uint16_t sbits;
+            quant128_quad<GROUP, BITS>(v, words, sbits);
+            uint4 *dst = reinterpret_cast<uint4 *>(codes + t * CB + q * (CB / 4));
+#pragma unroll
+            for (int i = 0; i < BITS / 4; ++i) st_global_v4(dst + i, make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]));
+            if ((q % (GROUP / 32)) == 0) scales[t * SG + q / (GROUP / 32)] = sbits;
         }
     }
 }
@@ -93,46 +94,58 @@ __global__ void __launch_bounds__(kWarps * 32) unpack_kernel(const uint8_t *__re
                                                               int64_t ld_out) {
     constexpr int CB = 128 * BITS / 8;
     constexpr int SG = 128 / GROUP;
-    constexpr int LANES_PER_GROUP = GROUP / 4;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hs = blockIdx.y * kWarps + warp;
     if (hs >= 2 * heads) return;
     const int kvi = hs >= heads ? 1 : 0;
     const int h = hs - kvi * heads;
+    const int q = lane & 3;
     const uint8_t *codes = (kvi ? v_codes : k_codes) + static_cast<int64_t>(h) * cap * CB;
     const uint16_t *scales = (kvi ? v_scales : k_scales) + static_cast<int64_t>(h) * cap * SG;
-    __nv_bfloat16 *dst = out + static_cast<int64_t>(hs) * 128 + lane * 4;
-    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock;
+    __nv_bfloat16 *dst = out + static_cast<int64_t>(hs) * 128 + q * 32;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock + (lane >> 2);
 #pragma unroll 1
-    for (int u = 0; u < kTokensPerBlock; ++u) {
-        const int64_t t = t0 + u;
-        if (t >= n) break;
-        uint32_t packed;
-        if constexpr (BITS == 4) {
-            packed = reinterpret_cast<const uint16_t *>(codes + t * CB)[lane];
-        } else {
-            packed = reinterpret_cast<const uint32_t *>(codes + t * CB)[lane];
-        }
-        const float s = __half2float(__ushort_as_half(scales[t * SG + lane / LANES_PER_GROUP]));
-        float v[4];
+    for (int p = 0; p < kTokensPerBlock / kPass; ++p) {
+        const int64_t t = t0 + p * kPass;
+        // every lane of the quad takes part in the shuffles; rows past n are not stored
+        const bool live = t < n;
+        uint4 cw[BITS / 4];
+        float s = 0.0f;
+        if (live) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+            for (int i = 0; i < BITS / 4; ++i) cw[i] = ld_global_nc_v4(codes + t * CB + q * (CB / 4) + 16 * i);
+            s = __half2float(__ushort_as_half(scales[t * SG + q / (GROUP / 32)]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < BITS / 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const uint32_t word = (&cw[e / (32 / BITS) / 4].x)[(e / (32 / BITS)) % 4];
             int c;
             if constexpr (BITS == 4) {
-                c = static_cast<int>((packed >> (4 * j)) & 0xFu);
+                c = static_cast<int>((word >> (4 * (e % 8))) & 0xFu);
                 c = (c ^ 8) - 8;
             } else {
-                c = static_cast<int>(static_cast<int8_t>((packed >> (8 * j)) & 0xFFu));
+                c = static_cast<int>(static_cast<int8_t>((word >> (8 * (e % 4))) & 0xFFu));
             }
-            v[j] = static_cast<float>(c) * s;
+            v[e] = static_cast<float>(c) * s;
         }
-        rotate128_warp(v, lane);
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-        uint2 w;
-        w.x = *reinterpret_cast<const uint32_t *>(&lo);
-        w.y = *reinterpret_cast<const uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(dst + t * ld_out) = w;
+        rotate128_quad(v, lane);
+        if (live) {
+            uint4 *o = reinterpret_cast<uint4 *>(dst + t * ld_out);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * k], v[8 * i + 2 * k + 1]);
+                    w4[k] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+        }
     }
 }
 
