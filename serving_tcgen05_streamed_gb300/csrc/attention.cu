@@ -96,17 +96,16 @@ struct AttnParams {
 };
 
 // Staging buffers of packed codes (as they sit in the store: 128 consecutive
-// key rows of one head), filled by bulk copies.  Two stages for INT4-only
-// stores, one (sized for INT8) when a store may hold INT8 ranges.
-template <bool MIXED>
+// key rows of one head), filled by bulk copies: two 16 KB stages.  An INT4
+// tile's K and V codes (8 KB each) share one stage; an INT8 tile takes two
+// consecutive stages, K codes in the first and V codes in the second.  The
+// loader and the dequantisers walk the same running stage counter.
 struct Staging {
-    static constexpr int CB = MIXED ? 128 : 64;  // code bytes per key row, largest case
-    static constexpr int STAGES = MIXED ? 1 : 2;
-    static constexpr int KC = 0;
-    static constexpr int VC = KC + 128 * CB;
-    static constexpr int STAGE_BYTES = VC + 128 * CB;
+    static constexpr int STAGES = 2;
+    static constexpr int STAGE_BYTES = 16384;
     static constexpr int BYTES = STAGES * STAGE_BYTES;
 };
+__host__ __device__ constexpr int stages_of(int bits) { return bits == 8 ? 2 : 1; }
 
 // Dynamic shared memory, 1024-byte aligned (checked at run time): no slack.
 template <int GROUP, bool MIXED>
@@ -115,7 +114,7 @@ struct SmemLayout {
     static constexpr int K = Q + NQT * TILE_BYTES;        // KV_STAGES tiles
     static constexpr int V = K + KV_STAGES * TILE_BYTES;  // KV_STAGES tiles
     static constexpr int STG = V + KV_STAGES * TILE_BYTES;
-    static constexpr int BAR = STG + Staging<MIXED>::BYTES;
+    static constexpr int BAR = STG + Staging::BYTES;
     static constexpr int BYTES = BAR + 256;
 };
 
@@ -216,74 +215,83 @@ __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// The tile sequence walks the ranges in order; tile j of the sequence is
-// local tile j - tiles_before[g] of range g.
+// The tile sequence walks the ranges in order: tile j of the sequence is
+// local tile j - tiles_before[g] of range g.  Every role walks it with its own
+// cursor, one step per tile.
 struct TileRef {
-    int g;
+    int g;         // range
+    int lt;        // tile inside the range
     int64_t key0;  // first key (row) of the tile inside range g
     int valid;     // keys of the tile that exist (1..128)
 };
-__device__ __forceinline__ TileRef tile_ref(const AttnParams &p, int j) {
-    int g = 0;
-    while (g + 1 < p.ranges.n && j >= p.tiles_before[g + 1]) ++g;
-    TileRef t;
-    t.g = g;
-    t.key0 = static_cast<int64_t>(j - p.tiles_before[g]) * BKV;
-    const int64_t rem = p.ranges.r[g].len - t.key0;
-    t.valid = rem < BKV ? static_cast<int>(rem) : BKV;
-    return t;
-}
+struct TileCursor {
+    int g = 0, lt = 0;
+    __device__ __forceinline__ TileRef ref(const AttnParams &p) const {
+        TileRef t;
+        t.g = g;
+        t.lt = lt;
+        t.key0 = static_cast<int64_t>(lt) * BKV;
+        const int64_t rem = p.ranges.r[g].len - t.key0;
+        t.valid = rem < BKV ? static_cast<int>(rem) : BKV;
+        return t;
+    }
+    __device__ __forceinline__ void next(const AttnParams &p) {
+        if (++lt == p.tiles_before[g + 1] - p.tiles_before[g]) {
+            lt = 0;
+            ++g;
+        }
+    }
+};
 
 // A tile's decode work is split into units of 16 staged code bytes: unit u of
 // the tile's 2 x 128 x (code bytes per row / 16) units is K (first half) or
 // V (second half), key row rem / cpr, 16-byte column rem % cpr (cpr = 4 for
 // INT4, 8 for INT8).  Dequantiser d takes units d, d + 192, d + 384, ...; a
 // warp's 32 consecutive units are 512 contiguous staged bytes.
-template <bool MIXED>
+template <int BITS>
 struct UnitPlan {
-    static constexpr int MAX_UNITS = MIXED ? 11 : 6;  // ceil(2*128*cpr / 192)
+    static constexpr int LG = BITS == 8 ? 3 : 2;  // log2 of 16-byte code columns per key row
+    static constexpr int UH = 128 << LG;          // units per K (or V) tile
+    static constexpr int MAX_UNITS = (2 * UH + NUM_DQ_THREADS - 1) / NUM_DQ_THREADS;
 };
+constexpr int kMaxUnits = UnitPlan<8>::MAX_UNITS;
 
-// fp16 scale of each unit of dequantiser d for tile j (0 for rows past the
+// fp16 scale of each unit of dequantiser d for tile t (0 for rows past the
 // tile's valid keys), loaded straight from global memory one tile ahead: a
 // warp's loads cover contiguous bytes.
-template <int GROUP, bool MIXED>
-__device__ __forceinline__ void load_scales(const AttnParams &p, int head, int j, int d,
-                                            uint32_t (&sc)[UnitPlan<MIXED>::MAX_UNITS]) {
+template <int GROUP, int BITS>
+__device__ __forceinline__ void load_scales(const AttnParams &p, int head, const TileRef &t, int d,
+                                            uint32_t (&sc)[kMaxUnits]) {
+    using U = UnitPlan<BITS>;
     constexpr int SG = 128 / GROUP;
-    const TileRef t = tile_ref(p, j);
     const RangeDev &rg = p.ranges.r[t.g];
     const int64_t row0 = static_cast<int64_t>(head) * rg.cap + t.key0;
-    const int cpr = (MIXED && rg.bits == 8) ? 8 : 4;
-    const int uh = 128 * cpr;
 #pragma unroll
-    for (int i = 0; i < UnitPlan<MIXED>::MAX_UNITS; ++i) {
+    for (int i = 0; i < U::MAX_UNITS; ++i) {
         const int u = d + NUM_DQ_THREADS * i;
-        const int kv = u >= uh ? 1 : 0;
-        const int rem = u - kv * uh;
-        const int r = rem / cpr;
-        const int g = ((rem % cpr) * (128 / cpr)) / GROUP;
+        const int kv = u >= U::UH ? 1 : 0;
+        const int rem = u - kv * U::UH;
+        const int r = rem >> U::LG;
+        const int g = ((rem & ((1 << U::LG) - 1)) << (7 - U::LG)) / GROUP;  // column x dims per column / GROUP
         const uint16_t *base = kv ? rg.v_scales : rg.k_scales;
-        sc[i] = (u < 2 * uh && r < t.valid) ? static_cast<uint32_t>(__ldg(base + (row0 + r) * SG + g)) : 0u;
+        sc[i] = (u < 2 * U::UH && r < t.valid) ? static_cast<uint32_t>(__ldg(base + (row0 + r) * SG + g)) : 0u;
     }
 }
 
 // Decodes unit u of a staged tile into K^ or V^ ([key][dim], 128-byte
 // swizzle, dims permuted inside each 8-dim chunk); rows past `valid` become zeros.
-template <bool MIXED>
-__device__ __forceinline__ void decode_unit(const uint8_t *stg, int u, int bits, int valid, uint32_t scale,
-                                            uint8_t *k_tile, uint8_t *v_tile) {
-    using SL = Staging<MIXED>;
-    const int cpr = (MIXED && bits == 8) ? 8 : 4;
-    const int uh = 128 * cpr;
-    const int kv = u >= uh ? 1 : 0;
-    const int rem = u - kv * uh;
-    const int r = rem / cpr, cc = rem % cpr;
-    const uint4 w = *reinterpret_cast<const uint4 *>(stg + (kv ? SL::VC : SL::KC) + r * (16 * cpr) + cc * 16);
+template <int BITS>
+__device__ __forceinline__ void decode_unit(const uint8_t *stg_k, const uint8_t *stg_v, int u, int valid,
+                                            uint32_t scale, uint8_t *k_tile, uint8_t *v_tile) {
+    using U = UnitPlan<BITS>;
+    const int kv = u >= U::UH ? 1 : 0;
+    const int rem = u - kv * U::UH;
+    const int r = rem >> U::LG, cc = rem & ((1 << U::LG) - 1);
+    const uint4 w = *reinterpret_cast<const uint4 *>((kv ? stg_v : stg_k) + r * (16 << U::LG) + cc * 16);
     uint8_t *tile = kv ? v_tile : k_tile;
     const bool live = r < valid;
     const uint32_t s2 = h2_dup(static_cast<uint16_t>(scale));
-    if (!MIXED || bits == 4) {
+    if constexpr (BITS == 4) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // dims 32cc + 8k .. +7
             uint32_t o[4] = {0u, 0u, 0u, 0u};
@@ -306,6 +314,29 @@ __device__ __forceinline__ void decode_unit(const uint8_t *stg, int u, int bits,
     }
 }
 
+// Decodes the dequantiser's units of one tile: K units first (once the K^
+// stage is free), then V units (once the V^ stage is free).
+template <int BITS>
+__device__ __forceinline__ bool decode_tile(const uint8_t *stg_k, const uint8_t *stg_v, int d, int valid,
+                                            const uint32_t (&sc)[kMaxUnits], uint8_t *kt, uint8_t *vt,
+                                            uint64_t *k_empty, uint64_t *v_empty, uint32_t ph,
+                                            volatile int *abort_flag) {
+    using U = UnitPlan<BITS>;
+    if (!mbar_wait(k_empty, ph, abort_flag, &g_err_attn)) return false;
+    bool v_free = false;
+#pragma unroll
+    for (int i = 0; i < U::MAX_UNITS; ++i) {
+        const int u = d + NUM_DQ_THREADS * i;
+        if (u >= 2 * U::UH) break;
+        if (u >= U::UH && !v_free) {
+            if (!mbar_wait(v_empty, ph, abort_flag, &g_err_attn)) return false;
+            v_free = true;
+        }
+        decode_unit<BITS>(stg_k, stg_v, u, valid, sc[i], kt, vt);
+    }
+    return v_free || mbar_wait(v_empty, ph, abort_flag, &g_err_attn);
+}
+
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
     tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
     tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
@@ -318,7 +349,7 @@ template <int GROUP, bool MIXED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttnParams p) {
     using L = SmemLayout<GROUP, MIXED>;
-    using SL = Staging<MIXED>;
+    using SL = Staging;
     extern __shared__ __align__(1024) uint8_t smem[];
     if (smem_u32(smem) & 1023u) {  // the layout below assumes a 1024-byte aligned base
         if (threadIdx.x == 0) atomicOr(&g_err_attn, 2u);
@@ -456,19 +487,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------------------ bulk copies of the codes
             if (elect_one()) {
                 uint32_t armed = 0, armed_parity = 0;
-                for (int j = 0; j < T && !*abort_flag; ++j) {
-                    const int s = j % SL::STAGES;
-                    if (!mbar_wait(&stg_empty[s], ((j / SL::STAGES) & 1) ^ 1, abort_flag, &g_err_attn)) break;
-                    const TileRef tr = tile_ref(p, j);
+                int k = 0;  // running stage counter
+                TileCursor cur;
+                for (int j = 0; j < T && !*abort_flag; ++j, cur.next(p)) {
+                    const TileRef tr = cur.ref(p);
                     const RangeDev &rg = p.ranges.r[tr.g];
-                    const uint32_t cb = (MIXED && rg.bits == 8) ? 128u : 64u;
+                    const int bits = MIXED ? rg.bits : 4;
+                    const uint32_t cb = bits == 8 ? 128u : 64u;
                     const int64_t row0 = static_cast<int64_t>(head) * rg.cap + tr.key0;
-                    uint8_t *dst = sStg + s * SL::STAGE_BYTES;
-                    mbar_arrive_expect_tx(&stg_full[s], 2u * 128u * cb);
-                    bulk_load(dst + SL::KC, rg.k_codes + row0 * cb, 128u * cb, &stg_full[s]);
-                    bulk_load(dst + SL::VC, rg.v_codes + row0 * cb, 128u * cb, &stg_full[s]);
-                    armed |= 1u << s;
-                    armed_parity = (armed_parity & ~(1u << s)) | (static_cast<uint32_t>((j / SL::STAGES) & 1) << s);
+                    bool fine = true;
+                    for (int c = 0; c < stages_of(bits) && fine; ++c) {
+                        const int s = (k + c) % SL::STAGES;
+                        const uint32_t ph = static_cast<uint32_t>(((k + c) / SL::STAGES) & 1);
+                        fine = mbar_wait(&stg_empty[s], ph ^ 1u, abort_flag, &g_err_attn);
+                        if (!fine) break;
+                        uint8_t *dst = sStg + s * SL::STAGE_BYTES;
+                        if (bits == 4) {  // K and V codes share the stage
+                            mbar_arrive_expect_tx(&stg_full[s], 2u * 128u * cb);
+                            bulk_load(dst, rg.k_codes + row0 * cb, 128u * cb, &stg_full[s]);
+                            bulk_load(dst + 128 * cb, rg.v_codes + row0 * cb, 128u * cb, &stg_full[s]);
+                        } else {  // K codes in the first stage, V codes in the second
+                            mbar_arrive_expect_tx(&stg_full[s], 128u * cb);
+                            bulk_load(dst, (c == 0 ? rg.k_codes : rg.v_codes) + row0 * cb, 128u * cb, &stg_full[s]);
+                        }
+                        armed |= 1u << s;
+                        armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+                    }
+                    if (!fine) break;
+                    k += stages_of(bits);
                 }
                 // drain: the last copies have landed before the CTA exits
                 volatile int no_abort = 0;
@@ -505,38 +551,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
         }
         mbar_arrive(q_ready);
-        uint32_t sc[UnitPlan<MIXED>::MAX_UNITS];
-        if (ok && T > 0) load_scales<GROUP, MIXED>(p, head, 0, d, sc);
-        for (int j = 0; ok && j < T && !*abort_flag; ++j) {
+        uint32_t sc[kMaxUnits];
+        TileCursor cur, ahead;  // tile j, and tile j + 1 for the scale loads
+        auto prefetch_scales = [&]() {
+            const TileRef ta = ahead.ref(p);
+            if (!MIXED || p.ranges.r[ta.g].bits == 4) load_scales<GROUP, 4>(p, head, ta, d, sc);
+            else load_scales<GROUP, 8>(p, head, ta, d, sc);
+            ahead.next(p);
+        };
+        if (ok && T > 0) prefetch_scales();
+        int k = 0;  // running stage counter, as the loader's
+        for (int j = 0; ok && j < T && !*abort_flag; ++j, cur.next(p)) {
             const int st = j % KV_STAGES;
-            const int s = j % SL::STAGES;
             const uint32_t ph = ((j / KV_STAGES) & 1) ^ 1;
-            if (!mbar_wait(&stg_full[s], (j / SL::STAGES) & 1, abort_flag, &g_err_attn)) break;
-            const TileRef tr = tile_ref(p, j);
+            const TileRef tr = cur.ref(p);
             const int bits = MIXED ? p.ranges.r[tr.g].bits : 4;
-            const int uh = 128 * ((MIXED && bits == 8) ? 8 : 4);
-            const uint8_t *stg = sStg + s * SL::STAGE_BYTES;
+            const int s0 = k % SL::STAGES, s1 = (k + stages_of(bits) - 1) % SL::STAGES;
+            if (!mbar_wait(&stg_full[s0], (k / SL::STAGES) & 1, abort_flag, &g_err_attn)) break;
+            if (bits == 8 && !mbar_wait(&stg_full[s1], ((k + 1) / SL::STAGES) & 1, abort_flag, &g_err_attn)) break;
+            const uint8_t *stg_k = sStg + s0 * SL::STAGE_BYTES;
+            const uint8_t *stg_v = bits == 8 ? sStg + s1 * SL::STAGE_BYTES : stg_k + 8192;
             uint8_t *kt = sK + st * TILE_BYTES;
             uint8_t *vt = sV + st * TILE_BYTES;
-            bool fine = mbar_wait(&k_empty[st], ph, abort_flag, &g_err_attn);
-            bool v_free = false;
-#pragma unroll
-            for (int i = 0; i < UnitPlan<MIXED>::MAX_UNITS && fine; ++i) {
-                const int u = d + NUM_DQ_THREADS * i;
-                if (u >= 2 * uh) break;
-                if (u >= uh && !v_free) {
-                    fine = mbar_wait(&v_empty[st], ph, abort_flag, &g_err_attn);
-                    v_free = true;
-                    if (!fine) break;
-                }
-                decode_unit<MIXED>(stg, u, bits, tr.valid, sc[i], kt, vt);
-            }
-            if (fine && !v_free) fine = mbar_wait(&v_empty[st], ph, abort_flag, &g_err_attn);
+            const bool fine = (!MIXED || bits == 4)
+                                  ? decode_tile<4>(stg_k, stg_v, d, tr.valid, sc, kt, vt, &k_empty[st], &v_empty[st],
+                                                   ph, abort_flag)
+                                  : decode_tile<8>(stg_k, stg_v, d, tr.valid, sc, kt, vt, &k_empty[st], &v_empty[st],
+                                                   ph, abort_flag);
             if (!fine) break;
-            mbar_arrive(&stg_empty[s]);  // every staged byte of this tile has been read
+            mbar_arrive(&stg_empty[s0]);  // every staged byte of this tile has been read
+            if (bits == 8) mbar_arrive(&stg_empty[s1]);
+            k += stages_of(bits);
             fence_proxy_async_smem();
             mbar_arrive(&kv_full[st]);
-            if (j + 1 < T) load_scales<GROUP, MIXED>(p, head, j + 1, d, sc);
+            if (j + 1 < T) prefetch_scales();
         }
     }
     } else {
@@ -552,7 +600,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float l = 0.0f;       // running sum of p
         const float sl = p.scale_log2;
         bool ok = true;
-        for (int j = 0; j < T; ++j) {
+        TileCursor cur;
+        for (int j = 0; j < T; ++j, cur.next(p)) {
             // the wait result is made warp-uniform before any warp-collective TMEM access
             if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_flag, &g_err_attn))) {
                 ok = false;
@@ -561,7 +610,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld128(sa, sr);
-            const int valid = tile_ref(p, j).valid;
+            const int valid = cur.ref(p).valid;
             if (valid < BKV) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
