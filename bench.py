@@ -106,15 +106,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(gpus: int):
+def dist_setup(gpus: int, backend: str = "nccl"):
+    """One process per GPU (torchrun): returns (world, rank, local_rank).
+    Every rank runs its own independent block; the process group is used only
+    for barriers and for the max of the per-rank times."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
+    elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -126,12 +132,22 @@ def barrier(world):
 
 
 def max_over_ranks(world, v: float) -> float:
+    """The largest of the ranks' values (the job takes as long as its slowest rank)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(world: int, rank_ms_total: float, steps: int, flops_per_block: float) -> tuple[float, float]:
+    """(ms per step, whole-job TFLOP/s): every rank runs one block per step, the
+    step time is the slowest rank's."""
+    total = max_over_ranks(world, rank_ms_total)
+    ms = total / steps
+    return ms, world * flops_per_block / (ms * 1e-3) / 1e12
 
 
 # --------------------------------------------------------------------------- CPU oracle (reference arm / baseline)
@@ -297,10 +313,7 @@ def run_gpu(args, wl, world, rank, local):
     barrier(world)
     clocks = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    total_ms = max_over_ranks(world, total_ms)
-    ms_per_step = total_ms / args.steps
-    value = world * (fp + fa) / (ms_per_step * 1e-3) / 1e12
+    ms_per_step, value = job_value(world, sum(step_ms), args.steps, fp + fa)
     assert kvq.device_status() == kvq.KVQ_OK
 
     # ------------------------------------------------------------ end to end: host buffers in and out
