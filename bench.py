@@ -406,9 +406,11 @@ def run_sweep(args):
     hbm = float(peaks["hbm_gbs"])
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
     rows = []
-    for n in inputs.SWEEP_N:
+    sizes = args.sweep_n or inputs.SWEEP_N
+    groups = args.sweep_groups or inputs.SWEEP_GROUPS
+    for n in sizes:
         kv = inputs.sweep_kv(n, C, seed=0, device="cuda")
-        for g in inputs.SWEEP_GROUPS:
+        for g in groups:
             store = kvq.PackedKV.empty(n, C, g, 4, "cuda")
             out = torch.empty_like(kv)
             res = {}
@@ -434,7 +436,7 @@ def run_sweep(args):
         del kv
     assert kvq.device_status() == kvq.KVQ_OK
     best = max(rows, key=lambda r: r["pack_gbs"])
-    big = [r for r in rows if r["n"] == max(inputs.SWEEP_N) and r["group"] == 32][0]
+    big = max(rows, key=lambda r: (r["n"], r["group"] == 32))
     print(json.dumps({
         "metric": "kv_rotate_quant_pack bandwidth (BF16 K/V -> rotated INT4 + fp16 scales)", "value": big["pack_gbs"],
         "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
@@ -442,7 +444,7 @@ def run_sweep(args):
         "config": {"workload": "K/V [N, 2x7168] sweep", "l2": "flushed before every launch"},
         "roofline": {"kernel": "kv_rotate_quant_pack", "bound": "hbm", "achieved": big["pack_gbs"], "peak": hbm,
                      "unit": "GB/s", "frac": big["pack_gbs"] / hbm, "peak_source": f"{kind} hbm copy",
-                     "at": {"n": big["n"], "group": 32}},
+                     "at": {"n": big["n"], "group": big["group"]}},
         "best": best, "sweep": rows}), flush=True)
 
 
@@ -458,6 +460,10 @@ def main():
     ap.add_argument("--workload", choices=("h3_ref2va", "mid", "mixed", "sweep"), default="h3_ref2va",
                     help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling); "
                          "mixed: N=217,088 with INT8 conditioning ranges; sweep: pack/unpack bandwidth")
+    ap.add_argument("--sweep-n", type=int, nargs="+", default=None,
+                    help="sweep: token counts to run (default: 4,096 ... 262,144)")
+    ap.add_argument("--sweep-groups", type=int, nargs="+", default=None, choices=(32, 64, 128),
+                    help="sweep: group sizes to run (default: 32 64 128)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
