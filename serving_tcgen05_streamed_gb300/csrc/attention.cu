@@ -245,14 +245,38 @@ struct TileCursor {
 
 // A tile's decode work is split into units of 16 staged code bytes: unit u of
 // the tile's 2 x 128 x (code bytes per row / 16) units is K (first half) or
-// V (second half), key row rem / cpr, 16-byte column rem % cpr (cpr = 4 for
-// INT4, 8 for INT8).  Dequantiser d takes units d, d + 192, d + 384, ...; a
-// warp's 32 consecutive units are 512 contiguous staged bytes.
+// V (second half); rem = u mod (units per half) names a key row and a 16-byte
+// code column (cpr = 4 columns per row for INT4, 8 for INT8).  Dequantiser d
+// takes units d, d + 192, d + 384, ...; a warp's 32 consecutive units are 512
+// contiguous staged bytes (8 INT4 rows or 4 INT8 rows).
+//
+// 16-byte shared-memory accesses are served eight lanes at a time, and each
+// group of eight must touch eight different 16-byte bank positions to take one
+// pass.  Inside a warp the units are dealt to lanes so that both the 16-byte
+// code loads (row stride 64 or 128 bytes) and the swizzled operand stores
+// (position ((dims / 8) mod 8) xor (row mod 8)) of every group of eight lanes
+// fall on eight distinct positions:
+//   INT4: lanes 8p..8p+7 take rows {2a, 2a+1} x columns {0, 1} and rows
+//         {2b, 2b+1} x columns {2, 3}, {a, b} = {0, 1} xor (p & 1), in row
+//         block 4 (p >> 1);
+//   INT8: lanes 8p..8p+7 take columns 0..3 of one row and 4..7 of the other
+//         row of the pair 2 (p >> 1), {0, 1} in the order p & 1.
 template <int BITS>
 struct UnitPlan {
     static constexpr int LG = BITS == 8 ? 3 : 2;  // log2 of 16-byte code columns per key row
     static constexpr int UH = 128 << LG;          // units per K (or V) tile
     static constexpr int MAX_UNITS = (2 * UH + NUM_DQ_THREADS - 1) / NUM_DQ_THREADS;
+    // key row r and code column cc of unit rem of a half
+    static __device__ __forceinline__ void rc(int rem, int &r, int &cc) {
+        const int x = rem & 31, swap = ((x >> 2) ^ (x >> 3)) & 1;
+        if constexpr (BITS == 4) {
+            r = ((rem >> 5) << 3) + ((x >> 4) << 2) + (swap << 1) + (x & 1);
+            cc = ((x >> 1) & 1) | (((x >> 2) & 1) << 1);
+        } else {
+            r = ((rem >> 5) << 2) + ((x >> 4) << 1) + swap;
+            cc = x & 7;
+        }
+    }
 };
 constexpr int kMaxUnits = UnitPlan<8>::MAX_UNITS;
 
@@ -270,9 +294,9 @@ __device__ __forceinline__ void load_scales(const AttnParams &p, int head, const
     for (int i = 0; i < U::MAX_UNITS; ++i) {
         const int u = d + NUM_DQ_THREADS * i;
         const int kv = u >= U::UH ? 1 : 0;
-        const int rem = u - kv * U::UH;
-        const int r = rem >> U::LG;
-        const int g = ((rem & ((1 << U::LG) - 1)) << (7 - U::LG)) / GROUP;  // column x dims per column / GROUP
+        int r, cc;
+        U::rc(u - kv * U::UH, r, cc);
+        const int g = (cc << (7 - U::LG)) / GROUP;  // column x dims per column / GROUP
         const uint16_t *base = kv ? rg.v_scales : rg.k_scales;
         sc[i] = (u < 2 * U::UH && r < t.valid) ? static_cast<uint32_t>(__ldg(base + (row0 + r) * SG + g)) : 0u;
     }
@@ -285,8 +309,8 @@ __device__ __forceinline__ void decode_unit(const uint8_t *stg_k, const uint8_t 
                                             uint32_t scale, uint8_t *k_tile, uint8_t *v_tile) {
     using U = UnitPlan<BITS>;
     const int kv = u >= U::UH ? 1 : 0;
-    const int rem = u - kv * U::UH;
-    const int r = rem >> U::LG, cc = rem & ((1 << U::LG) - 1);
+    int r, cc;
+    U::rc(u - kv * U::UH, r, cc);
     const uint4 w = *reinterpret_cast<const uint4 *>((kv ? stg_v : stg_k) + r * (16 << U::LG) + cc * 16);
     uint8_t *tile = kv ? v_tile : k_tile;
     const bool live = r < valid;
