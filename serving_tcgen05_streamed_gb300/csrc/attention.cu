@@ -9,10 +9,16 @@
 // output is un-rotated once; `_online_combine` is the log-sum-exp merge that
 // the running softmax below performs tile by tile.
 //
-// One CTA = one head x 256 query rows, as two 128-row tiles A and B that
-// take turns on the tensor core (ping-pong): while the softmax of tile A
-// works on its scores, the tensor core runs tile B's P.V and next Q.K^T, and
-// the other way round.  16 warps in four warpgroups:
+// A cluster of two CTAs (a CTA pair on two SMs) works on one head and 512
+// query rows; each CTA owns 256 of them as two 128-row tiles A and B.  The
+// tensor core runs 256-row MMAs over the pair (tcgen05 cta_group::2): rows
+// 0-127 from the even CTA, 128-255 from the odd one, while the B operand is
+// split along N between the two SMs.  So each CTA decodes only half of every
+// K/V tile: keys 64r .. 64r+63 of K^ (all 128 dims) and dims 64r .. 64r+63 of
+// V^ (all 128 keys), r = the CTA's rank in the pair.  Tiles A and B take
+// turns on the tensor core (ping-pong): while the softmax of tile A works on
+// its scores, the tensor core runs tile B's P.V and next Q.K^T, and the other
+// way round.  16 warps per CTA in four warpgroups:
 //   WG0, WG1   softmax of tile A / B: one thread per query row; reads the S
 //              row from TMEM, keeps a running max in the log2 domain and
 //              rescales the output accumulator only when the row max grew by
@@ -22,34 +28,38 @@
 //              by the row sum, un-rotates the row with the 128-point fast
 //              Walsh-Hadamard transform in registers and stores it.
 //   WG2 + warps 14-15   dequantisers (192 threads): per 128-key tile, read
-//              the INT4 / INT8 codes from a shared-memory staging buffer and
-//              the fp16 scales from global memory (a tile ahead), decode them
-//              with integer bit tricks into FP16 (code * scale) and store K^
-//              and V^, both [key][dim], in the 128-byte-swizzled layout the
-//              tensor core reads (K^ as the K-major B operand of Q.K^T, V^ as
-//              the MN-major B operand of P.V^).  K^ is decoded as soon as the
-//              last Q.K^T of its stage has run, V^ once the last P.V^ has.
-//              The dims are permuted inside each 8-dim chunk (the order
-//              e0 e4 e1 e5 e2 e6 e3 e7 falls out of the nibble decode): Q is
-//              permuted the same way when it is converted, so Q.K^T is
-//              unchanged, and the output columns come out in the same order
-//              and are put back in the epilogue.  They also convert the BF16
-//              Q tiles to FP16 once.
-//   warp 12    TMA of the Q tiles, TMEM allocation and the single MMA thread.
-//   warp 13    bulk copies (TMA engine) of each tile's contiguous codes into
-//              the staging buffer, one tile ahead.
+//              the INT4 / INT8 codes of the CTA's halves from a shared-memory
+//              staging buffer and the fp16 scales from global memory (a tile
+//              ahead), decode them with integer bit tricks into FP16
+//              (code * scale) and store K^ and V^, both [key][dim], in the
+//              128-byte-swizzled layout the tensor core reads (K^ as the
+//              K-major B operand of Q.K^T, V^ as the MN-major B operand of
+//              P.V^).  K^ is decoded as soon as the last Q.K^T of its stage
+//              has run, V^ once the last P.V^ has.  The dims are permuted
+//              inside each 8-dim chunk (the order e0 e4 e1 e5 e2 e6 e3 e7
+//              falls out of the nibble decode): Q is permuted the same way
+//              when it is converted, so Q.K^T is unchanged, and the output
+//              columns come out in the same order and are put back in the
+//              epilogue.  They also convert the CTA's BF16 Q tiles to FP16 once.
+//   warp 12    TMA of the CTA's Q tiles, TMEM allocation (jointly with the
+//              peer CTA) and, in the even CTA, the single MMA thread.
+//   warp 13    bulk copies (TMA engine) of each tile's codes into the staging
+//              buffer, one tile ahead.
+// The MMA thread waits on barriers of the even CTA that the threads of both
+// CTAs arrive on; its commits arrive on the same barriers of both CTAs.
 // Registers are redistributed with setmaxnreg: 168 per softmax thread, 88
 // for the rest (512 threads x 128 at launch).
-// TMEM (512 columns): S_A, S_B, O_A, O_B, 128 columns each; P_t aliases the
-// first 64 columns of S_t.  tcgen05.mma instructions from one thread execute
-// in issue order, so S_t(j+1), issued after P_t(j).V^(j), overwrites P_t(j)
-// only after that MMA has read it; and the commit that signals S_t(j+1) also
-// covers P_t(j).V^(j), so O_t is final for tile j when the softmax sees S_t(j+1).
+// TMEM (512 columns per CTA): S_A, S_B, O_A, O_B, 128 columns each; P_t
+// aliases the first 64 columns of S_t.  tcgen05.mma instructions from one
+// thread execute in issue order, so S_t(j+1), issued after P_t(j).V^(j),
+// overwrites P_t(j) only after that MMA has read it; and the commit that
+// signals S_t(j+1) also covers P_t(j).V^(j), so O_t is final for tile j when
+// the softmax sees S_t(j+1).
 // Scores, the softmax and O are fp32; the MMA operands are FP16 (11-bit
 // significand: the rotation spreads values evenly, where BF16's 8 bits would
 // cost a noticeably higher error floor).  No split over keys: every query
-// row is computed by one CTA in one fixed order, so results do not depend on
-// how the queries are tiled or chunked.
+// row is computed by one CTA pair in one fixed order, so results do not
+// depend on how the queries are tiled or chunked.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -69,16 +79,21 @@ constexpr int BQT = 128;       // query rows per tile
 constexpr int NQT = 2;         // query tiles per CTA
 constexpr int BQ = BQT * NQT;  // query rows per CTA
 constexpr int BKV = 128;       // keys per tile
-constexpr int KV_STAGES = 2;   // K^ / V^T shared-memory stages
-constexpr int NUM_DQ_THREADS = 192;   // warps 8-11 and 14-15
-constexpr int NUM_SM_THREADS = 128;   // per query tile
+constexpr int KV_STAGES = 2;   // K^ / V^ shared-memory stages
+constexpr int NUM_DQ_THREADS = 192;  // warps 8-11 and 14-15
+constexpr int NUM_DQ_WARPS = NUM_DQ_THREADS / 32;
+constexpr int NUM_SM_WARPS = 4;  // per query tile
 constexpr int NUM_THREADS = 512;
 constexpr int WARP_MMA = 12, WARP_LOAD = 13;
 constexpr int REG_SOFTMAX = 168, REG_OTHER = 88;
 static_assert(2 * 128 * REG_SOFTMAX + 2 * 128 * REG_OTHER <= NUM_THREADS * 128,
               "register split exceeds the launch budget");
-constexpr int TILE_BYTES = 128 * 128 * 2;  // one 128x128 fp16 operand tile
-constexpr int HALF_BYTES = TILE_BYTES / 2;
+constexpr int Q_TILE_BYTES = 128 * 128 * 2;  // 128 rows x 128 dims, as two 64-dim halves
+constexpr int Q_HALF_BYTES = Q_TILE_BYTES / 2;
+constexpr int K_TILE_BYTES = 64 * 128 * 2;  // the CTA's 64 keys x 128 dims, as two 64-dim halves
+constexpr int K_HALF_BYTES = K_TILE_BYTES / 2;
+constexpr int V_TILE_BYTES = 128 * 64 * 2;  // 128 keys x the CTA's 64 dims
+constexpr uint16_t kPairMask = 0x3;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 __host__ __device__ constexpr uint32_t tm_s(int t) { return static_cast<uint32_t>(t * 128); }
@@ -95,34 +110,29 @@ struct AttnParams {
     int tiles_before[KVQ_MAX_RANGES + 1];
 };
 
-// Staging buffers of packed codes (as they sit in the store: 128 consecutive
-// key rows of one head), filled by bulk copies: two 16 KB stages.  An INT4
-// tile's K and V codes (8 KB each) share one stage; an INT8 tile takes two
-// consecutive stages, K codes in the first and V codes in the second.  The
-// loader and the dequantisers walk the same running stage counter.
+// Staging buffers of packed codes, filled by bulk copies: two 16 KB stages.
+// An INT4 tile takes one stage: the CTA's 64 K rows (4 KB) at offset 0 and
+// all 128 V rows (8 KB, of which the CTA decodes its half of each row) at
+// offset 4096.  An INT8 tile takes two consecutive stages: 64 K rows (8 KB)
+// in the first, 128 V rows (16 KB) in the second.  The loader and the
+// dequantisers walk the same running stage counter.
 struct Staging {
     static constexpr int STAGES = 2;
     static constexpr int STAGE_BYTES = 16384;
     static constexpr int BYTES = STAGES * STAGE_BYTES;
+    static constexpr int INT4_V_OFFSET = 4096;
 };
 __host__ __device__ constexpr int stages_of(int bits) { return bits == 8 ? 2 : 1; }
 
-// Dynamic shared memory, 1024-byte aligned (checked at run time): no slack.
-template <int GROUP, bool MIXED>
+// Dynamic shared memory, 1024-byte aligned (checked at run time).
 struct SmemLayout {
-    static constexpr int Q = 0;                           // NQT tiles
-    static constexpr int K = Q + NQT * TILE_BYTES;        // KV_STAGES tiles
-    static constexpr int V = K + KV_STAGES * TILE_BYTES;  // KV_STAGES tiles
-    static constexpr int STG = V + KV_STAGES * TILE_BYTES;
+    static constexpr int Q = 0;                             // NQT tiles
+    static constexpr int K = Q + NQT * Q_TILE_BYTES;        // KV_STAGES tiles
+    static constexpr int V = K + KV_STAGES * K_TILE_BYTES;  // KV_STAGES tiles
+    static constexpr int STG = V + KV_STAGES * V_TILE_BYTES;
     static constexpr int BAR = STG + Staging::BYTES;
     static constexpr int BYTES = BAR + 256;
 };
-
-// Physical byte offset of 16-byte chunk `c` (0..15 along K) of row `r` in a
-// 128-row K-major tile stored as two 64-element halves, 128-byte swizzle.
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-    return static_cast<uint32_t>((c >> 3) * HALF_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
@@ -243,31 +253,35 @@ struct TileCursor {
     }
 };
 
-// A tile's decode work is split into units of 16 staged code bytes: unit u of
-// the tile's 2 x 128 x (code bytes per row / 16) units is K (first half) or
-// V (second half); rem = u mod (units per half) names a key row and a 16-byte
-// code column (cpr = 4 columns per row for INT4, 8 for INT8).  Dequantiser d
-// takes units d, d + 192, d + 384, ...; a warp's 32 consecutive units are 512
-// contiguous staged bytes (8 INT4 rows or 4 INT8 rows).
+// A tile's decode work in one CTA is split into units of 16 staged code
+// bytes: UK units of the CTA's 64 K rows (all 128 dims: cpr = 4 columns of
+// 16 bytes per row for INT4, 8 for INT8), then UV units of the CTA's half of
+// the 128 V rows (cpr / 2 columns per row).  Dequantiser d takes units d,
+// d + 192, d + 384, ...; a warp's 32 consecutive units are all K or all V.
 //
 // 16-byte shared-memory accesses are served eight lanes at a time, and each
-// group of eight must touch eight different 16-byte bank positions to take one
-// pass.  Inside a warp the units are dealt to lanes so that both the 16-byte
-// code loads (row stride 64 or 128 bytes) and the swizzled operand stores
-// (position ((dims / 8) mod 8) xor (row mod 8)) of every group of eight lanes
-// fall on eight distinct positions:
+// group of eight takes one pass when it touches eight different 16-byte bank
+// positions.  K units are dealt to lanes so that both the code loads (row
+// stride 64 or 128 bytes) and the swizzled operand stores (position
+// ((dims / 8) mod 8) xor (row mod 8)) of every group of eight lanes fall on
+// eight distinct positions:
 //   INT4: lanes 8p..8p+7 take rows {2a, 2a+1} x columns {0, 1} and rows
 //         {2b, 2b+1} x columns {2, 3}, {a, b} = {0, 1} xor (p & 1), in row
 //         block 4 (p >> 1);
 //   INT8: lanes 8p..8p+7 take columns 0..3 of one row and 4..7 of the other
 //         row of the pair 2 (p >> 1), {0, 1} in the order p & 1.
+// V units go row-major (four rows x two columns, or two rows x four columns,
+// per group of eight): conflict-free stores, two-way conflicting loads, as
+// only half of each staged V row is read.
 template <int BITS>
 struct UnitPlan {
     static constexpr int LG = BITS == 8 ? 3 : 2;  // log2 of 16-byte code columns per key row
-    static constexpr int UH = 128 << LG;          // units per K (or V) tile
-    static constexpr int MAX_UNITS = (2 * UH + NUM_DQ_THREADS - 1) / NUM_DQ_THREADS;
-    // key row r and code column cc of unit rem of a half
-    static __device__ __forceinline__ void rc(int rem, int &r, int &cc) {
+    static constexpr int UK = 64 << LG;           // K units
+    static constexpr int UV = 128 << (LG - 1);    // V units
+    static constexpr int MAX_UNITS = (UK + UV + NUM_DQ_THREADS - 1) / NUM_DQ_THREADS;
+    static constexpr int CPC = BITS == 8 ? 2 : 4;  // 8-dim chunks per 16-byte column
+    // key row r (0..63) and code column cc of K unit rem
+    static __device__ __forceinline__ void k_rc(int rem, int &r, int &cc) {
         const int x = rem & 31, swap = ((x >> 2) ^ (x >> 3)) & 1;
         if constexpr (BITS == 4) {
             r = ((rem >> 5) << 3) + ((x >> 4) << 2) + (swap << 1) + (x & 1);
@@ -277,14 +291,18 @@ struct UnitPlan {
             cc = x & 7;
         }
     }
+    // key row r (0..127) and code column c2 (0 .. cpr/2 - 1, inside the CTA's half) of V unit rem
+    static __device__ __forceinline__ void v_rc(int rem, int &r, int &c2) {
+        r = rem >> (LG - 1);
+        c2 = rem & ((1 << (LG - 1)) - 1);
+    }
 };
 constexpr int kMaxUnits = UnitPlan<8>::MAX_UNITS;
 
 // fp16 scale of each unit of dequantiser d for tile t (0 for rows past the
-// tile's valid keys), loaded straight from global memory one tile ahead: a
-// warp's loads cover contiguous bytes.
+// tile's valid keys), loaded straight from global memory one tile ahead.
 template <int GROUP, int BITS>
-__device__ __forceinline__ void load_scales(const AttnParams &p, int head, const TileRef &t, int d,
+__device__ __forceinline__ void load_scales(const AttnParams &p, int head, uint32_t rank, const TileRef &t, int d,
                                             uint32_t (&sc)[kMaxUnits]) {
     using U = UnitPlan<BITS>;
     constexpr int SG = 128 / GROUP;
@@ -293,34 +311,62 @@ __device__ __forceinline__ void load_scales(const AttnParams &p, int head, const
 #pragma unroll
     for (int i = 0; i < U::MAX_UNITS; ++i) {
         const int u = d + NUM_DQ_THREADS * i;
-        const int kv = u >= U::UH ? 1 : 0;
-        int r, cc;
-        U::rc(u - kv * U::UH, r, cc);
+        int key, cc;
+        const uint16_t *base;
+        if (u < U::UK) {
+            U::k_rc(u, key, cc);
+            key += 64 * static_cast<int>(rank);
+            base = rg.k_scales;
+        } else {
+            int c2;
+            U::v_rc(u - U::UK, key, c2);
+            cc = (static_cast<int>(rank) << (U::LG - 1)) + c2;
+            base = rg.v_scales;
+        }
         const int g = (cc << (7 - U::LG)) / GROUP;  // column x dims per column / GROUP
-        const uint16_t *base = kv ? rg.v_scales : rg.k_scales;
-        sc[i] = (u < 2 * U::UH && r < t.valid) ? static_cast<uint32_t>(__ldg(base + (row0 + r) * SG + g)) : 0u;
+        sc[i] = (u < U::UK + U::UV && key < t.valid) ? static_cast<uint32_t>(__ldg(base + (row0 + key) * SG + g))
+                                                      : 0u;
     }
 }
 
-// Decodes unit u of a staged tile into K^ or V^ ([key][dim], 128-byte
-// swizzle, dims permuted inside each 8-dim chunk); rows past `valid` become zeros.
+// Decodes unit u of a staged tile into the CTA's K^ half ([64 keys][128
+// dims] as two 64-dim halves) or V^ half ([128 keys][64 dims]), 128-byte
+// swizzle, dims permuted inside each 8-dim chunk; rows past `valid` become zeros.
 template <int BITS>
 __device__ __forceinline__ void decode_unit(const uint8_t *stg_k, const uint8_t *stg_v, int u, int valid,
-                                            uint32_t scale, uint8_t *k_tile, uint8_t *v_tile) {
+                                            uint32_t rank, uint32_t scale, uint8_t *k_tile, uint8_t *v_tile) {
     using U = UnitPlan<BITS>;
-    const int kv = u >= U::UH ? 1 : 0;
-    int r, cc;
-    U::rc(u - kv * U::UH, r, cc);
-    const uint4 w = *reinterpret_cast<const uint4 *>((kv ? stg_v : stg_k) + r * (16 << U::LG) + cc * 16);
-    uint8_t *tile = kv ? v_tile : k_tile;
-    const bool live = r < valid;
+    constexpr int ROW_BYTES = 16 << U::LG;
+    const uint8_t *src;
+    uint8_t *dst;
+    uint32_t c0, r7;  // first 8-dim chunk of the unit inside its 128-byte row, row swizzle
+    bool live;
+    if (u < U::UK) {
+        int r, cc;
+        U::k_rc(u, r, cc);
+        src = stg_k + r * ROW_BYTES + cc * 16;
+        const int c = cc * U::CPC;  // 0..15 over the 128 dims
+        dst = k_tile + (c >> 3) * K_HALF_BYTES + r * 128;
+        c0 = static_cast<uint32_t>(c & 7);
+        r7 = static_cast<uint32_t>(r & 7);
+        live = 64 * static_cast<int>(rank) + r < valid;
+    } else {
+        int r, c2;
+        U::v_rc(u - U::UK, r, c2);
+        src = stg_v + r * ROW_BYTES + ((static_cast<int>(rank) << (U::LG - 1)) + c2) * 16;
+        dst = v_tile + r * 128;
+        c0 = static_cast<uint32_t>(c2 * U::CPC);  // 0..7 over the CTA's 64 dims
+        r7 = static_cast<uint32_t>(r & 7);
+        live = r < valid;
+    }
+    const uint4 w = *reinterpret_cast<const uint4 *>(src);
     const uint32_t s2 = h2_dup(static_cast<uint16_t>(scale));
     if constexpr (BITS == 4) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // dims 32cc + 8k .. +7
             uint32_t o[4] = {0u, 0u, 0u, 0u};
             if (live) dq_int4_word((&w.x)[k], s2, o);
-            *reinterpret_cast<uint4 *>(tile + sw128_off(r, 4 * cc + k)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(dst + (((c0 + k) ^ r7) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     } else {
 #pragma unroll
@@ -333,32 +379,33 @@ __device__ __forceinline__ void decode_unit(const uint8_t *stg_k, const uint8_t 
                 o[2] = dq_int8_pair(a, b, 0x0602u, s2);
                 o[3] = dq_int8_pair(a, b, 0x0703u, s2);
             }
-            *reinterpret_cast<uint4 *>(tile + sw128_off(r, 2 * cc + k)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(dst + (((c0 + k) ^ r7) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
 }
 
 // Decodes the dequantiser's units of one tile: K units first (once the K^
-// stage is free), then V units (once the V^ stage is free).
+// stage is free), then V units (once the V^ stage is free).  Every wait result
+// is made warp-uniform, so a warp leaves together.
 template <int BITS>
 __device__ __forceinline__ bool decode_tile(const uint8_t *stg_k, const uint8_t *stg_v, int d, int valid,
-                                            const uint32_t (&sc)[kMaxUnits], uint8_t *kt, uint8_t *vt,
-                                            uint64_t *k_empty, uint64_t *v_empty, uint32_t ph,
+                                            uint32_t rank, const uint32_t (&sc)[kMaxUnits], uint8_t *kt,
+                                            uint8_t *vt, uint64_t *k_empty, uint64_t *v_empty, uint32_t ph,
                                             volatile int *abort_flag) {
     using U = UnitPlan<BITS>;
-    if (!mbar_wait(k_empty, ph, abort_flag, &g_err_attn)) return false;
+    if (!__all_sync(0xffffffffu, mbar_wait(k_empty, ph, abort_flag, &g_err_attn))) return false;
     bool v_free = false;
 #pragma unroll
     for (int i = 0; i < U::MAX_UNITS; ++i) {
         const int u = d + NUM_DQ_THREADS * i;
-        if (u >= 2 * U::UH) break;
-        if (u >= U::UH && !v_free) {
-            if (!mbar_wait(v_empty, ph, abort_flag, &g_err_attn)) return false;
+        if (u >= U::UK + U::UV) break;
+        if (u >= U::UK && !v_free) {
+            if (!__all_sync(0xffffffffu, mbar_wait(v_empty, ph, abort_flag, &g_err_attn))) return false;
             v_free = true;
         }
-        decode_unit<BITS>(stg_k, stg_v, u, valid, sc[i], kt, vt);
+        decode_unit<BITS>(stg_k, stg_v, u, valid, rank, sc[i], kt, vt);
     }
-    return v_free || mbar_wait(v_empty, ph, abort_flag, &g_err_attn);
+    return v_free || __all_sync(0xffffffffu, mbar_wait(v_empty, ph, abort_flag, &g_err_attn));
 }
 
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
@@ -370,11 +417,12 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 }
 
 template <int GROUP, bool MIXED>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttnParams p) {
-    using L = SmemLayout<GROUP, MIXED>;
+    using L = SmemLayout;
     using SL = Staging;
     extern __shared__ __align__(1024) uint8_t smem[];
+    // Both CTAs of a pair see the same offsets, so both leave here or neither does.
     if (smem_u32(smem) & 1023u) {  // the layout below assumes a 1024-byte aligned base
         if (threadIdx.x == 0) atomicOr(&g_err_attn, 2u);
         return;
@@ -385,125 +433,131 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t *sStg = smem + L::STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
     uint64_t *q_tma = bars + 0;
-    uint64_t *q_ready = bars + 1;
-    uint64_t *kv_full = bars + 2;   // [KV_STAGES]
+    uint64_t *q_ready = bars + 1;   // even CTA: Q of both CTAs converted
+    uint64_t *kv_full = bars + 2;   // [KV_STAGES], even CTA: both CTAs' halves decoded
     uint64_t *k_empty = bars + 4;   // [KV_STAGES]: K^ stage read by its last Q.K^T
     uint64_t *s_full = bars + 6;    // [NQT]
-    uint64_t *p_full = bars + 8;    // [NQT]
+    uint64_t *p_full = bars + 8;    // [NQT], even CTA: P of both CTAs in TMEM
     uint64_t *pv_done = bars + 10;  // [NQT]
     uint64_t *stg_full = bars + 12;   // [SL::STAGES]
     uint64_t *stg_empty = bars + 14;  // [SL::STAGES]
     uint64_t *v_empty = bars + 16;    // [KV_STAGES]: V^ stage read by its last P.V^
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+    uint64_t *drain = bars + 18;      // even CTA: every MMA has completed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 19);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
     const int head = blockIdx.y;
     const int64_t q0 = static_cast<int64_t>(blockIdx.x) * BQ;
     const int T = p.total_tiles;
 
     if (threadIdx.x == 0) {
         mbar_init(q_tma, 1);
-        mbar_init(q_ready, NUM_DQ_THREADS);
+        mbar_init(q_ready, 2 * NUM_DQ_WARPS);
         for (int i = 0; i < KV_STAGES; ++i) {
-            mbar_init(&kv_full[i], NUM_DQ_THREADS);
+            mbar_init(&kv_full[i], 2 * NUM_DQ_WARPS);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < NQT; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], NUM_SM_THREADS);
+            mbar_init(&p_full[i], 2 * NUM_SM_WARPS);
             mbar_init(&pv_done[i], 1);
         }
         for (int i = 0; i < SL::STAGES; ++i) {
             mbar_init(&stg_full[i], 1);
             mbar_init(&stg_empty[i], NUM_DQ_THREADS);
         }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == WARP_MMA) {
-        tmem_alloc(tmem_slot, 512);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
     }
+    // the peer may arrive on this CTA's barriers only once they are initialised
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp >= 8) {
     setmaxnreg_dec<REG_OTHER>();  // WG2 and WG3, one instruction for both warpgroups
-    if (warp >= 12 && warp < 14) {
+    if (warp == WARP_MMA || warp == WARP_LOAD) {
         // ------------------------------------------------------------ warp 12: Q load + MMA issue
         if (warp == WARP_MMA) {
             if (elect_one()) {
                 prefetch_tmap(&tm_q);
-                mbar_arrive_expect_tx(q_tma, NQT * TILE_BYTES);
+                mbar_arrive_expect_tx(q_tma, NQT * Q_TILE_BYTES);
 #pragma unroll
                 for (int t = 0; t < NQT; ++t) {
                     const int y = static_cast<int>(q0) + t * BQT;
-                    tma_load_2d(sQ + t * TILE_BYTES, &tm_q, q_tma, head * 128, y);
-                    tma_load_2d(sQ + t * TILE_BYTES + HALF_BYTES, &tm_q, q_tma, head * 128 + 64, y);
+                    tma_load_2d(sQ + t * Q_TILE_BYTES, &tm_q, q_tma, head * 128, y);
+                    tma_load_2d(sQ + t * Q_TILE_BYTES + Q_HALF_BYTES, &tm_q, q_tma, head * 128 + 64, y);
                 }
-                constexpr uint32_t idesc = make_idesc_f16(128, 128, 0);
-                constexpr uint32_t idesc_pv = make_idesc_f16(128, 128, 0, 1);  // V^ [key][dim]: MN-major B
-                const uint32_t qa = smem_u32(sQ);
-                bool ok = mbar_wait(q_ready, 0, abort_flag, &g_err_attn);
-                tc_fence_after();
-                auto issue_s = [&](int j, int t) {  // S_t(j) = Q_t . K^_j^T
-                    const uint32_t kb = smem_u32(sK + (j % KV_STAGES) * TILE_BYTES);
-                    const uint32_t d = tmem + tm_s(t);
-                    const uint32_t q = qa + t * TILE_BYTES;
+                if (rank == 0) {
+                    constexpr uint32_t idesc = make_idesc_f16(256, 128, 0);
+                    constexpr uint32_t idesc_pv = make_idesc_f16(256, 128, 0, 1);  // V^ [key][dim]: MN-major B
+                    const uint32_t qa = smem_u32(sQ);
+                    bool ok = mbar_wait_cluster(q_ready, 0, abort_flag, &g_err_attn);
+                    tc_fence_after();
+                    auto issue_s = [&](int j, int t) {  // S_t(j) = Q_t . K^_j^T over the pair
+                        const uint32_t kb = smem_u32(sK + (j % KV_STAGES) * K_TILE_BYTES);
+                        const uint32_t d = tmem + tm_s(t);
+                        const uint32_t q = qa + t * Q_TILE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-                        mma_f16_ss(d, make_sdesc_sw128(q + off), make_sdesc_sw128(kb + off), idesc, k > 0);
-                    }
-                    mma_commit(&s_full[t]);
-                };
-                if (ok && T > 0) {
-                    ok = mbar_wait(&kv_full[0], 0, abort_flag, &g_err_attn);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_s(0, 0);
-                        issue_s(0, 1);
-                        mma_commit(&k_empty[0]);
-                    }
-                }
-                for (int j = 0; ok && j < T; ++j) {
-                    const int st = j % KV_STAGES;
-                    const uint32_t vb = smem_u32(sV + st * TILE_BYTES);
-                    for (int t = 0; t < NQT && ok; ++t) {
-                        // O_t += P_t(j) . V^_j, P_t read from TMEM (the first 64 columns of S_t)
-                        ok = mbar_wait(&p_full[t], j & 1, abort_flag, &g_err_attn);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {  // keys 16k .. 16k+15: 16 rows of V^
-                            mma_f16_ts(tmem + tm_o(t), tmem + tm_s(t) + k * 8,
-                                       make_sdesc_sw128_mn(vb + k * 2048, HALF_BYTES), idesc_pv,
-                                       (j > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < 8; ++k) {
+                            const uint32_t kin = (k & 3) * 32;
+                            mma_f16_ss_pair(d, make_sdesc_sw128(q + (k >> 2) * Q_HALF_BYTES + kin),
+                                            make_sdesc_sw128(kb + (k >> 2) * K_HALF_BYTES + kin), idesc, k > 0);
                         }
-                        mma_commit(&pv_done[t]);
-                        if (t == NQT - 1) mma_commit(&v_empty[st]);
-                        if (j + 1 < T) {
-                            if (t == 0) {
-                                ok = mbar_wait(&kv_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, abort_flag,
-                                               &g_err_attn);
-                                if (!ok) break;
-                                tc_fence_after();
+                        mma_commit_pair(&s_full[t], kPairMask);
+                    };
+                    if (ok && T > 0) {
+                        ok = mbar_wait_cluster(&kv_full[0], 0, abort_flag, &g_err_attn);
+                        if (ok) {
+                            tc_fence_after();
+                            issue_s(0, 0);
+                            issue_s(0, 1);
+                            mma_commit_pair(&k_empty[0], kPairMask);
+                        }
+                    }
+                    for (int j = 0; ok && j < T; ++j) {
+                        const int st = j % KV_STAGES;
+                        const uint32_t vb = smem_u32(sV + st * V_TILE_BYTES);
+                        for (int t = 0; t < NQT && ok; ++t) {
+                            // O_t += P_t(j) . V^_j, P_t read from TMEM (the first 64 columns of S_t)
+                            ok = mbar_wait_cluster(&p_full[t], j & 1, abort_flag, &g_err_attn);
+                            if (!ok) break;
+                            tc_fence_after();
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {  // keys 16k .. 16k+15: 16 rows of V^
+                                mma_f16_ts_pair(tmem + tm_o(t), tmem + tm_s(t) + k * 8,
+                                                make_sdesc_sw128_mn(vb + k * 2048, V_TILE_BYTES), idesc_pv,
+                                                (j > 0 || k > 0) ? 1u : 0u);
                             }
-                            issue_s(j + 1, t);
-                            if (t == NQT - 1) mma_commit(&k_empty[(j + 1) % KV_STAGES]);
+                            mma_commit_pair(&pv_done[t], kPairMask);
+                            if (t == NQT - 1) mma_commit_pair(&v_empty[st], kPairMask);
+                            if (j + 1 < T) {
+                                if (t == 0) {
+                                    ok = mbar_wait_cluster(&kv_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1,
+                                                           abort_flag, &g_err_attn);
+                                    if (!ok) break;
+                                    tc_fence_after();
+                                }
+                                issue_s(j + 1, t);
+                                if (t == NQT - 1) mma_commit_pair(&k_empty[(j + 1) % KV_STAGES], kPairMask);
+                            }
                         }
                     }
+                    // drain: every MMA this thread issued has completed before the pair tears down
+                    volatile int no_abort = 0;
+                    mma_commit_pair(drain, 0x1);
+                    mbar_wait(drain, 0, &no_abort, nullptr, 1000000000ull);
                 }
-                // drain: nothing this thread issued is still running when the CTA exits
                 volatile int no_abort = 0;
-                if (*abort_flag) {
-                    mma_commit(&pv_done[0]);
-                    mbar_wait(&pv_done[0], 0, &no_abort, nullptr, 1000000000ull);
-                }
                 mbar_wait(q_tma, 0, &no_abort, nullptr);
             }
             __syncwarp();
@@ -517,8 +571,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const TileRef tr = cur.ref(p);
                     const RangeDev &rg = p.ranges.r[tr.g];
                     const int bits = MIXED ? rg.bits : 4;
-                    const uint32_t cb = bits == 8 ? 128u : 64u;
+                    const uint32_t cb = bits == 8 ? 128u : 64u;  // code bytes per key row
                     const int64_t row0 = static_cast<int64_t>(head) * rg.cap + tr.key0;
+                    const uint8_t *ksrc = rg.k_codes + (row0 + 64 * static_cast<int64_t>(rank)) * cb;
+                    const uint8_t *vsrc = rg.v_codes + row0 * cb;
                     bool fine = true;
                     for (int c = 0; c < stages_of(bits) && fine; ++c) {
                         const int s = (k + c) % SL::STAGES;
@@ -527,12 +583,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!fine) break;
                         uint8_t *dst = sStg + s * SL::STAGE_BYTES;
                         if (bits == 4) {  // K and V codes share the stage
-                            mbar_arrive_expect_tx(&stg_full[s], 2u * 128u * cb);
-                            bulk_load(dst, rg.k_codes + row0 * cb, 128u * cb, &stg_full[s]);
-                            bulk_load(dst + 128 * cb, rg.v_codes + row0 * cb, 128u * cb, &stg_full[s]);
-                        } else {  // K codes in the first stage, V codes in the second
+                            mbar_arrive_expect_tx(&stg_full[s], 64u * cb + 128u * cb);
+                            bulk_load(dst, ksrc, 64u * cb, &stg_full[s]);
+                            bulk_load(dst + SL::INT4_V_OFFSET, vsrc, 128u * cb, &stg_full[s]);
+                        } else if (c == 0) {  // K codes in the first stage
+                            mbar_arrive_expect_tx(&stg_full[s], 64u * cb);
+                            bulk_load(dst, ksrc, 64u * cb, &stg_full[s]);
+                        } else {  // V codes in the second
                             mbar_arrive_expect_tx(&stg_full[s], 128u * cb);
-                            bulk_load(dst, (c == 0 ? rg.k_codes : rg.v_codes) + row0 * cb, 128u * cb, &stg_full[s]);
+                            bulk_load(dst, vsrc, 128u * cb, &stg_full[s]);
                         }
                         armed |= 1u << s;
                         armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
@@ -551,10 +610,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------ dequantisers (warps 8-11, 14-15)
         const int d = warp < 12 ? static_cast<int>(threadIdx.x) - 256 : static_cast<int>(threadIdx.x) - 448 + 128;
         // Q: BF16 -> FP16 in place, dims permuted e0 e4 e1 e5 e2 e6 e3 e7 within each 8-chunk
-        const bool ok = mbar_wait(q_tma, 0, abort_flag, &g_err_attn);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(q_tma, 0, abort_flag, &g_err_attn));
         if (ok) {
 #pragma unroll 2
-            for (int i = d; i < NQT * TILE_BYTES / 16; i += NUM_DQ_THREADS) {
+            for (int i = d; i < NQT * Q_TILE_BYTES / 16; i += NUM_DQ_THREADS) {
                 uint4 *c = reinterpret_cast<uint4 *>(sQ + i * 16);
                 const uint4 v = *c;
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -573,14 +632,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 *c = make_uint4(o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
+            __syncwarp();
+            // the even CTA's barrier, in the cluster window
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(q_ready), 0));
         }
-        mbar_arrive(q_ready);
         uint32_t sc[kMaxUnits];
         TileCursor cur, ahead;  // tile j, and tile j + 1 for the scale loads
         auto prefetch_scales = [&]() {
             const TileRef ta = ahead.ref(p);
-            if (!MIXED || p.ranges.r[ta.g].bits == 4) load_scales<GROUP, 4>(p, head, ta, d, sc);
-            else load_scales<GROUP, 8>(p, head, ta, d, sc);
+            if (!MIXED || p.ranges.r[ta.g].bits == 4) load_scales<GROUP, 4>(p, head, rank, ta, d, sc);
+            else load_scales<GROUP, 8>(p, head, rank, ta, d, sc);
             ahead.next(p);
         };
         if (ok && T > 0) prefetch_scales();
@@ -591,23 +652,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const TileRef tr = cur.ref(p);
             const int bits = MIXED ? p.ranges.r[tr.g].bits : 4;
             const int s0 = k % SL::STAGES, s1 = (k + stages_of(bits) - 1) % SL::STAGES;
-            if (!mbar_wait(&stg_full[s0], (k / SL::STAGES) & 1, abort_flag, &g_err_attn)) break;
-            if (bits == 8 && !mbar_wait(&stg_full[s1], ((k + 1) / SL::STAGES) & 1, abort_flag, &g_err_attn)) break;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&stg_full[s0], (k / SL::STAGES) & 1, abort_flag, &g_err_attn)))
+                break;
+            if (bits == 8 && !__all_sync(0xffffffffu, mbar_wait(&stg_full[s1], ((k + 1) / SL::STAGES) & 1,
+                                                                abort_flag, &g_err_attn)))
+                break;
             const uint8_t *stg_k = sStg + s0 * SL::STAGE_BYTES;
-            const uint8_t *stg_v = bits == 8 ? sStg + s1 * SL::STAGE_BYTES : stg_k + 8192;
-            uint8_t *kt = sK + st * TILE_BYTES;
-            uint8_t *vt = sV + st * TILE_BYTES;
+            const uint8_t *stg_v = bits == 8 ? sStg + s1 * SL::STAGE_BYTES : stg_k + SL::INT4_V_OFFSET;
+            uint8_t *kt = sK + st * K_TILE_BYTES;
+            uint8_t *vt = sV + st * V_TILE_BYTES;
             const bool fine = (!MIXED || bits == 4)
-                                  ? decode_tile<4>(stg_k, stg_v, d, tr.valid, sc, kt, vt, &k_empty[st], &v_empty[st],
-                                                   ph, abort_flag)
-                                  : decode_tile<8>(stg_k, stg_v, d, tr.valid, sc, kt, vt, &k_empty[st], &v_empty[st],
-                                                   ph, abort_flag);
+                                  ? decode_tile<4>(stg_k, stg_v, d, tr.valid, rank, sc, kt, vt, &k_empty[st],
+                                                   &v_empty[st], ph, abort_flag)
+                                  : decode_tile<8>(stg_k, stg_v, d, tr.valid, rank, sc, kt, vt, &k_empty[st],
+                                                   &v_empty[st], ph, abort_flag);
             if (!fine) break;
             mbar_arrive(&stg_empty[s0]);  // every staged byte of this tile has been read
             if (bits == 8) mbar_arrive(&stg_empty[s1]);
             k += stages_of(bits);
             fence_proxy_async_smem();
-            mbar_arrive(&kv_full[st]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&kv_full[st]), 0));
             if (j + 1 < T) prefetch_scales();
         }
     }
@@ -705,7 +771,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int c = 0; c < 4; ++c) tmem_st16(sa + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[t]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&p_full[t]), 0));
         }
         // epilogue: O / l, un-rotate, store
         if (ok && T > 0 && __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (T - 1) & 1, abort_flag, &g_err_attn))) {
@@ -750,15 +817,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
+    // neither CTA of the pair leaves (or frees TMEM) while the other may still
+    // arrive on its barriers or the MMAs may still touch its memory
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
-    if (warp == WARP_MMA) tmem_dealloc(tmem, 512);
+    if (warp == WARP_MMA) tmem_dealloc_pair(tmem, 512);
 }
 
 template <int GROUP, bool MIXED>
 int launch_one(const CUtensorMap &tm, const AttnParams &p, dim3 grid, cudaStream_t s) {
-    constexpr int smem = SmemLayout<GROUP, MIXED>::BYTES;
+    constexpr int smem = SmemLayout::BYTES;
     auto fn = attention_kernel<GROUP, MIXED>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) {
@@ -797,7 +866,9 @@ int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int h
     }
     p.tiles_before[ranges.n] = tiles;
     p.total_tiles = tiles;
-    dim3 grid(static_cast<unsigned>((n_q + BQ - 1) / BQ), static_cast<unsigned>(hidden / 128));
+    // CTA pairs: an even number of CTAs of BQ query rows each
+    const int64_t pairs = (n_q + 2 * BQ - 1) / (2 * BQ);
+    dim3 grid(static_cast<unsigned>(2 * pairs), static_cast<unsigned>(hidden / 128));
     if (group == 32) return launch_group<32>(tm_q, p, grid, mixed, s);
     if (group == 64) return launch_group<64>(tm_q, p, grid, mixed, s);
     return launch_group<128>(tm_q, p, grid, mixed, s);
