@@ -443,7 +443,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint64_t *stg_empty = bars + 14;  // [SL::STAGES]
     uint64_t *v_empty = bars + 16;    // [KV_STAGES]: V^ stage read by its last P.V^
     uint64_t *drain = bars + 18;      // even CTA: every MMA has completed
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 19);
+    uint64_t *p_half = bars + 19;     // [NQT], even CTA: P of keys 0-63 of both CTAs in TMEM
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 21);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -463,6 +464,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < NQT; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 2 * NUM_SM_WARPS);
+            mbar_init(&p_half[i], 2 * NUM_SM_WARPS);
             mbar_init(&pv_done[i], 1);
         }
         for (int i = 0; i < SL::STAGES; ++i) {
@@ -528,16 +530,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                         const int st = j % KV_STAGES;
                         const uint32_t vb = smem_u32(sV + st * V_TILE_BYTES);
                         for (int t = 0; t < NQT && ok; ++t) {
-                            // O_t += P_t(j) . V^_j, P_t read from TMEM (the first 64 columns of S_t)
-                            ok = mbar_wait_cluster(&p_full[t], j & 1, abort_flag, &g_err_attn);
-                            if (!ok) break;
-                            tc_fence_after();
+                            // O_t += P_t(j) . V^_j, P_t read from TMEM (the first 64 columns of S_t);
+                            // keys 0-63 go as soon as their P is written, keys 64-127 after
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) {  // keys 16k .. 16k+15: 16 rows of V^
-                                mma_f16_ts_pair(tmem + tm_o(t), tmem + tm_s(t) + k * 8,
-                                                make_sdesc_sw128_mn(vb + k * 2048, V_TILE_BYTES), idesc_pv,
-                                                (j > 0 || k > 0) ? 1u : 0u);
+                            for (int hf = 0; hf < 2; ++hf) {
+                                ok = mbar_wait_cluster(hf == 0 ? &p_half[t] : &p_full[t], j & 1, abort_flag,
+                                                       &g_err_attn);
+                                if (!ok) break;
+                                tc_fence_after();
+#pragma unroll
+                                for (int k = 4 * hf; k < 4 * hf + 4; ++k) {  // keys 16k .. 16k+15: 16 rows of V^
+                                    mma_f16_ts_pair(tmem + tm_o(t), tmem + tm_s(t) + k * 8,
+                                                    make_sdesc_sw128_mn(vb + k * 2048, V_TILE_BYTES), idesc_pv,
+                                                    (j > 0 || k > 0) ? 1u : 0u);
+                                }
                             }
+                            if (!ok) break;
                             mma_commit_pair(&pv_done[t], kPairMask);
                             if (t == NQT - 1) mma_commit_pair(&v_empty[st], kPairMask);
                             if (j + 1 < T) {
@@ -725,54 +733,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 m = cand;
             }
             const bool rescale = __any_sync(0xffffffffu, grow);
-            // p = 2^(s*sl - m) as FP16 pairs, packed over S's first 64 columns
+            // p = 2^(s*sl - m) as FP16 pairs, packed over S's first 64 columns, in two
+            // halves of 64 keys: the MMA starts on keys 0-63 while keys 64-127 are computed
             const uint64_t sl2 = f2_pack(sl, sl), nm2 = f2_pack(-m, -m);
             uint64_t acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
-            uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                const uint64_t a0 = f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2, nm2);
-                const uint64_t a1 =
-                    f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2, nm2);
-                float x0, x1, x2, x3;
-                f2_unpack(a0, x0, x1);
-                f2_unpack(a1, x2, x3);
-                x0 = ex2_approx(x0);
-                x1 = ex2_approx(x1);
-                x2 = ex2_approx(x2);
-                x3 = ex2_approx(x3);
-                const __half2 h0 = __floats2half2_rn(x0, x1);
-                const __half2 h1 = __floats2half2_rn(x2, x3);
-                pk[c >> 1] = *reinterpret_cast<const uint32_t *>(&h0);
-                pk[(c >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h1);
-                // the row sum takes the fp32 weights (the MMA sees them rounded to FP16,
-                // a relative 2^-12 per weight that averages out in the sum)
-                acc0 = f2_add(acc0, f2_pack(x0, x1));
-                acc1 = f2_add(acc1, f2_pack(x2, x3));
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 64 * hf; c < 64 * hf + 64; c += 4) {
+                    const uint64_t a0 =
+                        f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2, nm2);
+                    const uint64_t a1 =
+                        f2_fma(f2_pack(__uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3])), sl2, nm2);
+                    float x0, x1, x2, x3;
+                    f2_unpack(a0, x0, x1);
+                    f2_unpack(a1, x2, x3);
+                    x0 = ex2_approx(x0);
+                    x1 = ex2_approx(x1);
+                    x2 = ex2_approx(x2);
+                    x3 = ex2_approx(x3);
+                    const __half2 h0 = __floats2half2_rn(x0, x1);
+                    const __half2 h1 = __floats2half2_rn(x2, x3);
+                    pk[(c - 64 * hf) >> 1] = *reinterpret_cast<const uint32_t *>(&h0);
+                    pk[((c - 64 * hf) >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+                    // the row sum takes the fp32 weights (the MMA sees them rounded to FP16,
+                    // a relative 2^-12 per weight that averages out in the sum)
+                    acc0 = f2_add(acc0, f2_pack(x0, x1));
+                    acc1 = f2_add(acc1, f2_pack(x2, x3));
+                }
+                // S_t(j) completing implies P_t(j-1).V^(j-1) completed: O_t is final for
+                // j-1 and is rescaled before the first P_t(j).V^(j) is issued
+                if (hf == 0 && rescale && j > 0) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 128; c0 += 32) {
+                        uint32_t o32[32];
+                        tmem_ld32(oa + c0, o32);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+                        tmem_st16(oa + c0, *reinterpret_cast<const uint32_t(*)[16]>(&o32[0]));
+                        tmem_st16(oa + c0 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o32[16]));
+                    }
+                }
+                tmem_st16(sa + 32 * hf, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+                tmem_st16(sa + 32 * hf + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+                tmem_st_wait();  // also covers the O rescale above
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(hf == 0 ? &p_half[t] : &p_full[t]), 0));
             }
             float u0, u1, u2, u3;
             f2_unpack(acc0, u0, u1);
             f2_unpack(acc1, u2, u3);
             l = l * alpha + ((u0 + u1) + (u2 + u3));
-            // S_t(j) completing implies P_t(j-1).V^(j-1) completed: O_t is final for j-1
-            if (rescale && j > 0) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    uint32_t o32[32];
-                    tmem_ld32(oa + c0, o32);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
-                    tmem_st16(oa + c0, *reinterpret_cast<const uint32_t(*)[16]>(&o32[0]));
-                    tmem_st16(oa + c0 + 16, *reinterpret_cast<const uint32_t(*)[16]>(&o32[16]));
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_st16(sa + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[c * 16]));
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&p_full[t]), 0));
         }
         // epilogue: O / l, un-rotate, store
         if (ok && T > 0 && __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (T - 1) & 1, abort_flag, &g_err_attn))) {
