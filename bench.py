@@ -348,7 +348,8 @@ def run_gpu(args, wl, world, rank, local):
             rec = json.load(f)
         src = os.path.join(ROOT, "serving_tcgen05_streamed_gb300", "csrc", "attention.cu")
         with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() == rec.get("source_sha256"):
+            if (hashlib.sha256(f.read()).hexdigest() == rec.get("source_sha256")
+                    and rec.get("workload") == wl.name):
                 traffic = rec.get("bytes_per_launch")
 
     cpu = None
