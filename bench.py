@@ -32,6 +32,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
+E2E_IN_CHUNK = 16384   # tokens per host-to-device chunk of x in the end-to-end step
+E2E_OUT_CHUNK = 19456  # query rows per attention launch in the end-to-end step (38 CTA pairs)
 METRIC = "block TFLOP/s + tokens/s (QKV GEMM + INT4-KV attn) at N=152,263; peak GiB"
 GiB = 2.0 ** 30
 
@@ -317,20 +319,60 @@ def run_gpu(args, wl, world, rank, local):
     assert kvq.device_status() == kvq.KVQ_OK
 
     # ------------------------------------------------------------ end to end: host buffers in and out
+    # Each step copies x in from pinned host memory and the attention output back.
+    # The copies run on their own stream and overlap the kernels: x goes in by token
+    # chunks, each chunk projected (through a row window of the store) as soon as it
+    # has landed; the attention runs by query chunks, each chunk's output copied back
+    # while the next is computed.  Results are those of the one-call path (rows are
+    # independent in the projection; the attention does not depend on query tiling).
     x_host = x.cpu().pin_memory()
     out_host = torch.empty((n, C), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
+    copy = torch.cuda.Stream(device=dev)
+    in_chunks = [(s0, min(E2E_IN_CHUNK, n - s0)) for s0 in range(0, n, E2E_IN_CHUNK)]
+    out_chunks = [(s0, min(E2E_OUT_CHUNK, n - s0)) for s0 in range(0, n, E2E_OUT_CHUNK)]
+
+    def windows(s0, length):  # the stores' rows of tokens s0 .. s0+length-1, in order
+        out, start = [], 0
+        for st_ in stores:
+            a, b = max(s0, start), min(s0 + length, start + st_.n)
+            if a < b:
+                out.append(st_.rows(a - start, b - a))
+            start += st_.n
+        return out
+
+    def e2e_step():
+        landed = []
+        with torch.cuda.stream(copy):
+            for s0, ln in in_chunks:
+                x_dev[s0:s0 + ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy)
+                landed.append(ev)
+        for (s0, ln), ev in zip(in_chunks, landed):
+            stream.wait_event(ev)
+            kvq.streamed_qkv_proj_mixed(x_dev[s0:s0 + ln], w, windows(s0, ln), group=32, chunk_tokens=wl.chunk_tokens,
+                                        q_norm_w=qn, k_norm_w=kn, q_out=q[s0:s0 + ln], stream=stream)
+        for s0, ln in out_chunks:
+            qc = q[s0:s0 + ln]
+            if mixed:
+                kvq.packed_kv_attention_mixed(qc, stores, out=qc, stream=stream)
+            else:
+                kvq.packed_kv_attention(qc, store, out=qc, stream=stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            copy.wait_event(ev)
+            with torch.cuda.stream(copy):
+                out_host[s0:s0 + ln].copy_(qc, non_blocking=True)
+        torch.cuda.synchronize()
+
     e2e_steps = max(1, min(args.steps, 3))
     for i in range(1 + e2e_steps):
         if i == 1:
             torch.cuda.synchronize()
             barrier(world)
             t0 = time.perf_counter()
-        x_dev.copy_(x_host, non_blocking=True)
-        project(x_dev)
-        attend()
-        out_host.copy_(q, non_blocking=True)
-        torch.cuda.synchronize()
+        e2e_step()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     e2e_s = max_over_ranks(world, e2e_s)
     e2e_val = world * (fp + fa) / e2e_s / 1e12
@@ -385,7 +427,8 @@ def run_gpu(args, wl, world, rank, local):
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(x.numel() * 2),
                     "d2h_bytes_per_step": int(n * C * 2),
-                    "note": "x copied in from pinned host memory and the attention output copied back each step; "
+                    "note": "x copied in from pinned host memory and the attention output copied back each step, "
+                            "on a copy stream overlapping the kernels (token chunks in, query chunks out); "
                             "W stays resident"},
             "gpu_launches": 2 * args.steps,
             "cpu_baseline": cpu,

@@ -124,6 +124,14 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _whole_store(store: "PackedKV", what: str):
+    # the single-store calls take the head stride from n; a row window (PackedKV.rows)
+    # goes through the range-table calls, which take it explicitly
+    if store.cap != padded_rows(store.n):
+        raise ValueError(f"{what}: store rows per head {store.cap} != padded_rows(n) {padded_rows(store.n)}; "
+                         "pass row windows to the *_mixed calls")
+
+
 def _need_cuda(*ts):
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -143,7 +151,16 @@ class PackedKV:
 
     @property
     def cap(self) -> int:
-        return self.k_codes.shape[1]
+        """Rows per head in memory (the head stride), also for a row window."""
+        return self.k_codes.stride(0) // self.k_codes.stride(1)
+
+    def rows(self, start: int, length: int) -> "PackedKV":
+        """Window of `length` token rows starting at `start` of every head, sharing
+        this store's memory (a projection over a token chunk writes into it)."""
+        assert 0 <= start and start + length <= self.n
+        sl = lambda t: t[:, start:start + length]  # noqa: E731
+        return PackedKV(sl(self.k_codes), sl(self.v_codes), sl(self.k_scales), sl(self.v_scales), length, self.bits,
+                        self.group)
 
     @property
     def heads(self) -> int:
@@ -171,6 +188,7 @@ def kv_rotate_quant_pack(kv: torch.Tensor, hidden: int, group: int = 32, bits: i
     assert kv.dtype == torch.bfloat16 and kv.dim() == 2 and kv.stride(1) == 1
     n = kv.shape[0]
     out = PackedKV.empty(n, hidden, group, bits, kv.device) if out is None else out
+    _whole_store(out, "kv_rotate_quant_pack")
     st = load().kv_rotate_quant_pack(_ptr(kv), n, hidden, kv.stride(0), group, bits, _ptr(out.k_codes),
                                      _ptr(out.v_codes), _ptr(out.k_scales), _ptr(out.v_scales), _stream(stream))
     _check(st, "kv_rotate_quant_pack")
@@ -180,6 +198,7 @@ def kv_rotate_quant_pack(kv: torch.Tensor, hidden: int, group: int = 32, bits: i
 def kv_unpack(store: PackedKV, hidden: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Packed store -> BF16 K/V [n, 2*hidden] (diagnostic; materialises K/V)."""
     _need_cuda(store.k_codes)
+    _whole_store(store, "kv_unpack")
     n = store.n
     out = torch.empty((n, 2 * hidden), dtype=torch.bfloat16, device=store.k_codes.device) if out is None else out
     st = load().kv_unpack(_ptr(store.k_codes), _ptr(store.v_codes), _ptr(store.k_scales), _ptr(store.v_scales), n,
@@ -197,6 +216,7 @@ def streamed_qkv_proj(x: torch.Tensor, w_qkv: torch.Tensor, group: int = 32, chu
     n, C = x.shape
     q_out = torch.empty((n, C), dtype=torch.bfloat16, device=x.device) if q_out is None else q_out
     store = PackedKV.empty(n, C, group, 4, x.device) if store is None else store
+    _whole_store(store, "streamed_qkv_proj")
     st = load().streamed_qkv_proj(_ptr(x), _ptr(w_qkv), n, C, group, chunk_tokens, _ptr(q_norm_w), _ptr(k_norm_w),
                                   eps, _ptr(q_out), _ptr(store.k_codes), _ptr(store.v_codes), _ptr(store.k_scales),
                                   _ptr(store.v_scales), _stream(stream))
@@ -209,6 +229,7 @@ def packed_kv_attention(q: torch.Tensor, store: PackedKV, sm_scale: float = 0.0,
     """q BF16 [n_q, C] (rotated) against an INT4 store -> out [n_q, C] (BF16 or fp32).
     `out` may be `q` itself for BF16 output."""
     _need_cuda(q, store.k_codes)
+    _whole_store(store, "packed_kv_attention")
     n_q, C = q.shape
     if out is None:
         out = torch.empty((n_q, C), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)

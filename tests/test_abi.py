@@ -119,3 +119,16 @@ def test_python_binding_refuses_cpu_tensors():
     x = torch.zeros((4, 256), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         kvq.kv_rotate_quant_pack(x, 128)
+
+
+def test_store_row_window_keeps_the_head_stride():
+    # a row window shares the store's memory and reports the whole store's rows per
+    # head, which the range-table calls take as the head stride
+    st = kvq.PackedKV.empty(1000, 512, 32, 4, "cpu")
+    assert st.cap == kvq.padded_rows(1000) == 1024
+    win = st.rows(256, 300)
+    assert win.n == 300 and win.cap == 1024 and win.heads == 4
+    assert win.k_codes.data_ptr() - st.k_codes.data_ptr() == 256 * 64
+    assert win.k_scales.data_ptr() - st.k_scales.data_ptr() == 256 * 4 * 2
+    win.v_codes[1, 0, 0] = 7
+    assert st.v_codes[1, 256, 0] == 7

@@ -110,6 +110,30 @@ def test_results_do_not_depend_on_chunk_size():
             assert torch.equal(a, b)
 
 
+def test_token_chunks_through_store_windows_match_one_call():
+    # the end-to-end path projects token chunks into row windows of one store;
+    # rows are independent, so every byte equals the one-call result (ragged last chunk)
+    x, w, qn, kn = inputs.block_inputs(inputs.TINY)
+    x = x.cuda()
+    w = w.cuda()
+    n, C = x.shape
+    n = n - 37  # a ragged tail
+    x = x[:n]
+    q0, s0 = kvq.streamed_qkv_proj(x, w)
+    store = kvq.PackedKV.empty(n, C, 32, 4, "cuda")
+    q1 = torch.empty_like(q0)
+    for s in range(0, n, 256):
+        ln = min(256, n - s)
+        win = store.rows(s, ln)
+        assert win.cap == store.cap
+        kvq.streamed_qkv_proj_mixed(x[s:s + ln], w, [win], q_out=q1[s:s + ln])
+    torch.cuda.synchronize()
+    assert torch.equal(q0, q1)
+    for a, b in ((s0.k_codes, store.k_codes), (s0.v_codes, store.v_codes), (s0.k_scales, store.k_scales),
+                 (s0.v_scales, store.v_scales)):
+        assert torch.equal(a[:, :n], b[:, :n])
+
+
 def test_h3_block_with_rmsnorm_sampled_rows():
     # H3 width (7168, 56 heads), Q/K RMSNorm, chunk 4096; the oracle checks sampled rows
     wl = inputs.MID
