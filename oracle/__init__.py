@@ -71,6 +71,8 @@ def _load():
             lib.kvqo_qkv_proj.argtypes = [P, P, I, P, I64, I, I, P, P, F, P, P, P, P, P, P]
             lib.kvqo_attention.restype = I
             lib.kvqo_attention.argtypes = [P, I64, I, P, P, P, P, I64, I64, I, I, F, P, I64, P]
+            lib.kvqo_attention_causal.restype = I
+            lib.kvqo_attention_causal.argtypes = [P, I64, I, P, P, P, P, I64, I64, I, I, F, I64, P, I64, P]
             lib.kvqo_attention_mixed.restype = I
             lib.kvqo_attention_mixed.argtypes = [P, I64, I, I, P, P, P, P, P, P, P, P, I, F, P, I64, P]
             lib.kvqo_threads.restype = I
@@ -228,6 +230,27 @@ def attention(q, k_codes, v_codes, k_scales, v_scales, *, n_kv: int, group: int 
                                 _p(rows), len(rows), _p(out))
     if rc:
         raise ValueError("oracle attention: bad arguments")
+    return out
+
+
+def attention_causal(q, k_codes, v_codes, k_scales, v_scales, *, n_kv: int, q_pos0: int = 0, group: int = 32,
+                     bits: int = 4, sm_scale: float | None = None, rows=None) -> np.ndarray:
+    """As attention(), with query row i at key position q_pos0 + i attending
+    keys j <= q_pos0 + i only."""
+    q = _c(q, np.uint16)
+    n_q, C = q.shape
+    heads = C // HD
+    kc, vc = _c(k_codes, np.uint8), _c(v_codes, np.uint8)
+    ks, vs = _c(k_scales, np.uint16), _c(v_scales, np.uint16)
+    n_pad = kc.shape[1]
+    assert kc.shape[0] == heads and ks.shape[:2] == (heads, n_pad)
+    rows = np.arange(n_q, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    sm = HD ** -0.5 if sm_scale is None else sm_scale
+    out = np.empty((len(rows), C), np.float32)
+    rc = _load().kvqo_attention_causal(_p(q), C, heads, _p(kc), _p(vc), _p(ks), _p(vs), n_kv, n_pad, group, bits, sm,
+                                       int(q_pos0), _p(rows), len(rows), _p(out))
+    if rc:
+        raise ValueError("oracle causal attention: bad arguments")
     return out
 
 

@@ -386,6 +386,49 @@ int kvqo_attention(const uint16_t *q, int64_t ldq, int heads, const uint8_t *k_c
     return 0;
 }
 
+/* Causal attention over the same store (a reading: the pages only name a
+ * general packed-K/V attention primitive, [I] "Proposed backend capability";
+ * the causal form is the standard prefix mask).  Listed row i sits at key
+ * position q_pos0 + i and attends keys j <= q_pos0 + i, j < n_kv, which is
+ * the attention above over the prefix of min(n_kv, q_pos0 + i + 1) keys.
+ * q_pos0 >= 0, so every row sees key 0. */
+int kvqo_attention_causal(const uint16_t *q, int64_t ldq, int heads, const uint8_t *k_codes, const uint8_t *v_codes,
+                          const uint16_t *k_scales, const uint16_t *v_scales, int64_t n_kv, int64_t n_pad, int group,
+                          int bits, float sm_scale, int64_t q_pos0, const int64_t *rows, int64_t n_rows, float *out) {
+    if (check_fmt(heads * HD, group, bits) || n_kv < 1 || n_pad < n_kv || q_pos0 < 0) return 1;
+    const int cb = HD * bits / 8, sg = HD / group, C = heads * HD;
+    float *Kd = (float *)malloc(sizeof(float) * (size_t)n_kv * HD);
+    float *Vd = (float *)malloc(sizeof(float) * (size_t)n_kv * HD);
+    if (!Kd || !Vd) {
+        free(Kd);
+        free(Vd);
+        return 2;
+    }
+    for (int h = 0; h < heads; ++h) {
+#pragma omp parallel for schedule(static)
+        for (int64_t j = 0; j < n_kv; ++j) {
+            int64_t t = (int64_t)h * n_pad + j;
+            kvqo_dequant_head(k_codes + t * cb, k_scales + t * sg, group, bits, Kd + j * HD);
+            kvqo_dequant_head(v_codes + t * cb, v_scales + t * sg, group, bits, Vd + j * HD);
+        }
+#pragma omp parallel
+        {
+            double *p = (double *)malloc(sizeof(double) * (size_t)n_kv);
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < n_rows; ++r) {
+                float qf[HD];
+                for (int d = 0; d < HD; ++d) qf[d] = kvqo_bf16_to_f32(q[rows[r] * ldq + h * HD + d]);
+                const int64_t vis = q_pos0 + rows[r] + 1;
+                attend_head(qf, Kd, Vd, vis < n_kv ? vis : n_kv, sm_scale, out + r * C + h * HD, p);
+            }
+            free(p);
+        }
+    }
+    free(Kd);
+    free(Vd);
+    return 0;
+}
+
 /* Mixed-precision store ([I] "Mixed precision for conditioning": chosen
  * token ranges at INT8, the rest at rotated INT4).  Each of the n_ranges
  * ranges [start, start+len) has its own head-major store of `bits` (4 or 8)

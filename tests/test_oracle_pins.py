@@ -332,6 +332,64 @@ def test_attention_matches_brute_force(bits):
     assert np.max(np.abs(got - ref)) < 1e-5 * max(1.0, np.abs(ref).max())
 
 
+def _brute_attention_causal(q_bits, kc, vc, ks, vs, n_kv, q_pos0, group, bits, sm_scale):
+    """Independent brute force of the prefix (causal) mask: the full score
+    matrix plus -inf above the shifted diagonal, scipy softmax, float64."""
+    heads = kc.shape[0]
+    nq = q_bits.shape[0]
+    q = oracle.bf16_to_f32(q_bits).astype(np.float64).reshape(nq, heads, HD)
+
+    def deq(codes, scales):
+        v = _unpack_nibbles(codes) if bits == 4 else codes.view(np.int8).astype(np.int16)
+        return v.astype(np.float64) * np.repeat(scales.view(np.float16).astype(np.float64), group, axis=-1)
+
+    mask = np.where(np.arange(n_kv)[None, :] > (q_pos0 + np.arange(nq))[:, None], -np.inf, 0.0)
+    out = np.empty_like(q)
+    for h in range(heads):
+        K = deq(kc[h, :n_kv], ks[h, :n_kv])
+        V = deq(vc[h, :n_kv], vs[h, :n_kv])
+        P = scipy.special.softmax(q[:, h] @ K.T * sm_scale + mask, axis=-1)
+        out[:, h] = (P @ V) @ H.T
+    return out.reshape(nq, -1)
+
+
+@pytest.mark.parametrize("bits,q_pos0", [(4, 0), (4, 5), (8, 150), (4, 180)])
+def test_attention_causal_matches_masked_brute_force(bits, q_pos0):
+    from serving_tcgen05_streamed_gb300 import inputs
+    heads, n, n_pad, nq = 2, 200, 256, 37
+    kc, vc, ks, vs = [t.numpy() for t in inputs.random_packed_kv(heads, n, n_pad, 32, bits, seed=21)]
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    q = _bf16_bits(inputs.random_q(nq, heads * HD, seed=22, std=2.0))
+    got = oracle.attention_causal(q, kc, vc, ks, vs, n_kv=n, q_pos0=q_pos0, group=32, bits=bits)
+    ref = _brute_attention_causal(q, kc, vc, ks, vs, n, q_pos0, 32, bits, HD ** -0.5)
+    assert np.max(np.abs(got - ref)) < 1e-5 * max(1.0, np.abs(ref).max())
+
+
+def test_attention_causal_closed_forms_and_limits():
+    from serving_tcgen05_streamed_gb300 import inputs
+    heads, n, nq = 1, 64, 8
+    kc, vc, ks, vs = [t.numpy() for t in inputs.random_packed_kv(heads, n, n, 32, 4, seed=23)]
+    ks, vs = ks.view(np.uint16), vs.view(np.uint16)
+    q = _bf16_bits(inputs.random_q(nq, HD, seed=24, std=2.0))
+    # position 0 sees key 0 alone: its value, un-rotated
+    out = oracle.attention_causal(q, kc, vc, ks, vs, n_kv=n, q_pos0=0)
+    v0 = oracle.dequant_head(vc[0, 0], vs[0, 0], 32, 4).astype(np.float64) @ H
+    assert np.allclose(out[0], v0, atol=1e-6)
+    # positions past the last key see every key: the unmasked attention, bit for bit
+    full = oracle.attention(q, kc, vc, ks, vs, n_kv=n)
+    assert np.array_equal(oracle.attention_causal(q, kc, vc, ks, vs, n_kv=n, q_pos0=n - 1), full)
+    # a mask on key j changes nothing for rows that cannot see it: perturbing the
+    # last key leaves every row at a position before it unchanged
+    kc2 = kc.copy()
+    kc2[0, n - 1] ^= 0x77
+    a = oracle.attention_causal(q, kc, vc, ks, vs, n_kv=n, q_pos0=20)
+    b = oracle.attention_causal(q, kc2, vc, ks, vs, n_kv=n, q_pos0=20)
+    assert np.array_equal(a, b)
+    # row sampling returns the same rows
+    rows = np.array([7, 0, 3], np.int64)
+    assert np.array_equal(oracle.attention_causal(q, kc, vc, ks, vs, n_kv=n, q_pos0=20, rows=rows), a[rows])
+
+
 def test_attention_closed_forms():
     heads, C = 1, 128
     r = _rng(8)
