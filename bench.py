@@ -38,9 +38,9 @@ METRIC = "block TFLOP/s + tokens/s (QKV GEMM + INT4-KV attn) at N=152,263; peak 
 GiB = 2.0 ** 30
 
 
-def flops(n: int, C: int) -> tuple[float, float]:
-    """(projection FLOPs, attention FLOPs) of one block."""
-    return 2.0 * n * C * 3 * C, 4.0 * n * n * C
+def flops(n: int, C: int, causal: bool = False) -> tuple[float, float]:
+    """(projection FLOPs, attention FLOPs) of one block; causal: row i sees i + 1 keys."""
+    return 2.0 * n * C * 3 * C, (2.0 * n * (n + 1) * C if causal else 4.0 * n * n * C)
 
 
 def load_peaks():
@@ -259,7 +259,9 @@ def run_gpu(args, wl, world, rank, local):
     x, w, qn, kn = inputs.block_inputs(wl, device=dev)
     if world > 1:  # independent problems per rank
         x = x.roll(rank * 7, dims=0)
-    fp, fa = flops(n, C)
+    causal = args.workload == "causal"
+    wl_label = wl.name + (", causal attention" if causal else "")
+    fp, fa = flops(n, C, causal)
 
     mixed = wl is inputs.MIXED
     if mixed:  # INT8 for the conditioning ranges, rotated INT4 for the generated video
@@ -282,6 +284,8 @@ def run_gpu(args, wl, world, rank, local):
     def attend():
         if mixed:
             kvq.packed_kv_attention_mixed(q, stores, out=q, stream=stream)
+        elif causal:
+            kvq.packed_kv_attention_causal(q, store, out=q, stream=stream)
         else:
             kvq.packed_kv_attention(q, store, out=q, stream=stream)
 
@@ -357,6 +361,8 @@ def run_gpu(args, wl, world, rank, local):
             qc = q[s0:s0 + ln]
             if mixed:
                 kvq.packed_kv_attention_mixed(qc, stores, out=qc, stream=stream)
+            elif causal:
+                kvq.packed_kv_attention_causal(qc, store, q_pos0=s0, out=qc, stream=stream)
             else:
                 kvq.packed_kv_attention(qc, store, out=qc, stream=stream)
             ev = torch.cuda.Event()
@@ -391,11 +397,11 @@ def run_gpu(args, wl, world, rank, local):
         src = os.path.join(ROOT, "serving_tcgen05_streamed_gb300", "csrc", "attention.cu")
         with open(src, "rb") as f:
             if (hashlib.sha256(f.read()).hexdigest() == rec.get("source_sha256")
-                    and rec.get("workload") == wl.name):
+                    and rec.get("workload") == wl_label):
                 traffic = rec.get("bytes_per_launch")
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not mixed:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not mixed and not causal:
         del x_host, out_host, x_dev
         sample = CpuOracleSample(wl, seed=7, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
         t_block = sample.run()
@@ -408,7 +414,8 @@ def run_gpu(args, wl, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 GEMM / fp16 attention operands, fp32 accumulate",
             "data": "synthetic (seeded generators; random-init weights of the H3 block shape)",
-            "config": {"workload": wl.name, "n_tokens": n, "hidden": C, "heads": wl.heads, "group": 32,
+            "config": {"workload": wl_label, "n_tokens": n, "hidden": C,
+                       "heads": wl.heads, "group": 32, "causal": causal,
                        "kv_bits": "8/4 by token range" if mixed else 4, "chunk_tokens": wl.chunk_tokens,
                        "qk_rmsnorm": True,
                        "l2": f"inputs larger than L2 (x {n * C * 2 / GiB:.2f} GiB, packed K/V "
@@ -501,9 +508,10 @@ def main():
     ap.add_argument("--ref-proj-rows", type=int, default=16)
     ap.add_argument("--ref-attn-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("h3_ref2va", "mid", "mixed", "sweep"), default="h3_ref2va",
+    ap.add_argument("--workload", choices=("h3_ref2va", "mid", "mixed", "causal", "sweep"), default="h3_ref2va",
                     help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling); "
-                         "mixed: N=217,088 with INT8 conditioning ranges; sweep: pack/unpack bandwidth")
+                         "mixed: N=217,088 with INT8 conditioning ranges; causal: the N=152,263 block with causal "
+                         "attention; sweep: pack/unpack bandwidth")
     ap.add_argument("--sweep-n", type=int, nargs="+", default=None,
                     help="sweep: token counts to run (default: 4,096 ... 262,144)")
     ap.add_argument("--sweep-groups", type=int, nargs="+", default=None, choices=(32, 64, 128),
@@ -515,7 +523,8 @@ def main():
     if args.workload == "sweep":
         run_sweep(args)
         return
-    wl = {"h3_ref2va": inputs.H3_REF2VA, "mid": inputs.MID, "mixed": inputs.MIXED}[args.workload]
+    wl = {"h3_ref2va": inputs.H3_REF2VA, "mid": inputs.MID, "mixed": inputs.MIXED,
+          "causal": inputs.H3_REF2VA}[args.workload]
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, wl, int(os.environ.get("WORLD_SIZE", "1")), rank)

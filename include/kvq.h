@@ -141,6 +141,20 @@ KVQ_API int packed_kv_attention(const void *q, int64_t n_q, const void *k_codes,
                         const void *v_scales, int64_t n_kv, int hidden, int group, float sm_scale, int out_fp32,
                         void *out, kvq_stream_t stream);
 
+/* Causal form of packed_kv_attention.  The pages name a general packed-K/V
+ * attention primitive ("Proposed backend capability"); the causal form is
+ * the usual prefix mask.  Query row i sits at key position q_pos0 + i and
+ * attends keys j <= q_pos0 + i (j < n_kv); q_pos0 >= 0, so every row sees key
+ * 0.  A query chunk [a, a + m) of a sequence attends with q pointing at row a
+ * and q_pos0 = a, and gives the rows of the one-call result.  Arguments,
+ * layouts, aliasing and errors as packed_kv_attention, plus KVQ_ERR_ARG for
+ * q_pos0 < 0.  Work is about half of the unmasked call when q_pos0 = 0 and
+ * n_q = n_kv (key tiles past a CTA pair's last row are skipped). */
+KVQ_API int packed_kv_attention_causal(const void *q, int64_t n_q, int64_t q_pos0, const void *k_codes,
+                               const void *v_codes, const void *k_scales, const void *v_scales, int64_t n_kv,
+                               int hidden, int group, float sm_scale, int out_fp32, void *out,
+                               kvq_stream_t stream);
+
 /* ---------------------------------------------------------------- a6: mixed precision by token range
  * ("Mixed precision for conditioning": text / reference / audio ranges at
  * INT8, generated video at rotated INT4.)  Every range holds its own K and V
@@ -148,8 +162,11 @@ KVQ_API int packed_kv_attention(const void *q, int64_t n_q, const void *k_codes,
  * of its arrays); token t of the sequence is row t - start of the range that
  * holds it.  Ranges must be given in order and tile [0, n) exactly, at most
  * KVQ_MAX_RANGES of them.  INT8 ranges use the same rotation, so Q and the
- * output need no per-range handling; rows len..cap-1 of a store are zeroed by
- * the projection. */
+ * output need no per-range handling.  The projection also writes the rows
+ * of the last range from len up to the next multiple of 128 (the codes of
+ * zero rows); no other row past len is touched, so a range may be a window
+ * (pointers advanced by the window's first row, cap the store's head stride)
+ * into a larger store. */
 typedef struct kvq_range {
     int64_t start;
     int64_t len;

@@ -25,7 +25,8 @@ KVQ_OK, KVQ_ERR_ARG, KVQ_ERR_ALIGN, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_T
 EXPORTS = (
     "kvq_status_str", "kvq_version", "kvq_padded_rows", "kvq_codes_bytes", "kvq_scales_bytes",
     "kv_rotate_quant_pack", "kv_unpack", "streamed_qkv_proj", "packed_kv_attention",
-    "streamed_qkv_proj_mixed", "packed_kv_attention_mixed", "kvq_device_status", "kvq_selftest_wait_timeout",
+    "packed_kv_attention_causal", "streamed_qkv_proj_mixed", "packed_kv_attention_mixed", "kvq_device_status",
+    "kvq_selftest_wait_timeout",
 )
 
 
@@ -77,6 +78,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.streamed_qkv_proj.argtypes = [P, P, I64, I, I, I64, P, P, F, P, P, P, P, P, P]
         lib.packed_kv_attention.restype = I
         lib.packed_kv_attention.argtypes = [P, I64, P, P, P, P, I64, I, I, F, I, P, P]
+        lib.packed_kv_attention_causal.restype = I
+        lib.packed_kv_attention_causal.argtypes = [P, I64, I64, P, P, P, P, I64, I, I, F, I, P, P]
         lib.streamed_qkv_proj_mixed.restype = I
         lib.streamed_qkv_proj_mixed.argtypes = [P, P, I64, I, I, I64, P, P, F, P, ctypes.POINTER(_Range), I, P]
         lib.packed_kv_attention_mixed.restype = I
@@ -237,6 +240,23 @@ def packed_kv_attention(q: torch.Tensor, store: PackedKV, sm_scale: float = 0.0,
                                     _ptr(store.v_scales), store.n, C, store.group, sm_scale, int(out_fp32),
                                     _ptr(out), _stream(stream))
     _check(st, "packed_kv_attention")
+    return out
+
+
+def packed_kv_attention_causal(q: torch.Tensor, store: PackedKV, q_pos0: int = 0, sm_scale: float = 0.0,
+                               out_fp32: bool = False, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal form: query row i sits at key position q_pos0 + i and attends keys
+    j <= q_pos0 + i.  A query chunk starting at row a of a sequence passes
+    q = rows a.. and q_pos0 = a."""
+    _need_cuda(q, store.k_codes)
+    _whole_store(store, "packed_kv_attention_causal")
+    n_q, C = q.shape
+    if out is None:
+        out = torch.empty((n_q, C), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)
+    st = load().packed_kv_attention_causal(_ptr(q), n_q, int(q_pos0), _ptr(store.k_codes), _ptr(store.v_codes),
+                                           _ptr(store.k_scales), _ptr(store.v_scales), store.n, C, store.group,
+                                           sm_scale, int(out_fp32), _ptr(out), _stream(stream))
+    _check(st, "packed_kv_attention_causal")
     return out
 
 

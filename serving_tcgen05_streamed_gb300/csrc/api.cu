@@ -105,6 +105,42 @@ int cuda_status(cudaError_t e) { return report_cuda(e, "launch"); }
 
 using namespace kvq;
 
+namespace {
+int attention_common(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges, int hidden, int group,
+                     float sm_scale, int out_fp32, void *out, kvq_stream_t stream, int causal, int64_t q_pos0) {
+    if (!q || !out) return KVQ_ERR_ARG;
+    if (n_q < 1 || n_q > (int64_t(1) << 31) - 256 || !valid_hidden(hidden) || !valid_group(group)) return KVQ_ERR_ARG;
+    if (out_fp32 != 0 && out_fp32 != 1) return KVQ_ERR_ARG;
+    if (out_fp32 && out == q) return KVQ_ERR_ARG;
+    if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
+    int64_t n_kv = 0;
+    if (ranges && n_ranges >= 1 && n_ranges <= KVQ_MAX_RANGES)
+        for (int i = 0; i < n_ranges; ++i) n_kv += ranges[i].len;
+    RangeTable t;
+    int st = check_range_table(ranges, n_ranges, n_kv, hidden, group, true, &t);
+    if (st) return st;
+    if (causal && q_pos0 < 0) return KVQ_ERR_ARG;
+    if (!(sm_scale > 0.0f)) sm_scale = 0.08838834764831845f;
+    return launch_attention(q, n_q, t, hidden, group, sm_scale, out_fp32, out, reinterpret_cast<cudaStream_t>(stream),
+                            causal, q_pos0);
+}
+
+int single_range(const void *k_codes, const void *v_codes, const void *k_scales, const void *v_scales, int64_t n_kv,
+                 kvq_range *r) {
+    if (n_kv < 1) return KVQ_ERR_ARG;
+    std::memset(r, 0, sizeof(*r));
+    r->start = 0;
+    r->len = n_kv;
+    r->cap = kvq_padded_rows(n_kv);
+    r->bits = 4;
+    r->k_codes = const_cast<void *>(k_codes);
+    r->v_codes = const_cast<void *>(v_codes);
+    r->k_scales = const_cast<void *>(k_scales);
+    r->v_scales = const_cast<void *>(v_scales);
+    return KVQ_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char *kvq_status_str(int status) {
@@ -198,38 +234,28 @@ int streamed_qkv_proj(const void *x, const void *w_qkv, int64_t n, int hidden, i
                                    stream);
 }
 
+
 int packed_kv_attention_mixed(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges, int hidden,
                               int group, float sm_scale, int out_fp32, void *out, kvq_stream_t stream) {
-    if (!q || !out) return KVQ_ERR_ARG;
-    if (n_q < 1 || n_q > (int64_t(1) << 31) - 256 || !valid_hidden(hidden) || !valid_group(group)) return KVQ_ERR_ARG;
-    if (out_fp32 != 0 && out_fp32 != 1) return KVQ_ERR_ARG;
-    if (out_fp32 && out == q) return KVQ_ERR_ARG;
-    if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_ALIGN;
-    int64_t n_kv = 0;
-    if (ranges && n_ranges >= 1 && n_ranges <= KVQ_MAX_RANGES)
-        for (int i = 0; i < n_ranges; ++i) n_kv += ranges[i].len;
-    RangeTable t;
-    int st = check_range_table(ranges, n_ranges, n_kv, hidden, group, true, &t);
-    if (st) return st;
-    if (!(sm_scale > 0.0f)) sm_scale = 0.08838834764831845f;
-    return launch_attention(q, n_q, t, hidden, group, sm_scale, out_fp32, out, reinterpret_cast<cudaStream_t>(stream));
+    return attention_common(q, n_q, ranges, n_ranges, hidden, group, sm_scale, out_fp32, out, stream, 0, 0);
 }
 
 int packed_kv_attention(const void *q, int64_t n_q, const void *k_codes, const void *v_codes, const void *k_scales,
                         const void *v_scales, int64_t n_kv, int hidden, int group, float sm_scale, int out_fp32,
                         void *out, kvq_stream_t stream) {
-    if (n_kv < 1) return KVQ_ERR_ARG;
     kvq_range r;
-    std::memset(&r, 0, sizeof(r));
-    r.start = 0;
-    r.len = n_kv;
-    r.cap = kvq_padded_rows(n_kv);
-    r.bits = 4;
-    r.k_codes = const_cast<void *>(k_codes);
-    r.v_codes = const_cast<void *>(v_codes);
-    r.k_scales = const_cast<void *>(k_scales);
-    r.v_scales = const_cast<void *>(v_scales);
-    return packed_kv_attention_mixed(q, n_q, &r, 1, hidden, group, sm_scale, out_fp32, out, stream);
+    const int st = single_range(k_codes, v_codes, k_scales, v_scales, n_kv, &r);
+    if (st) return st;
+    return attention_common(q, n_q, &r, 1, hidden, group, sm_scale, out_fp32, out, stream, 0, 0);
+}
+
+int packed_kv_attention_causal(const void *q, int64_t n_q, int64_t q_pos0, const void *k_codes, const void *v_codes,
+                               const void *k_scales, const void *v_scales, int64_t n_kv, int hidden, int group,
+                               float sm_scale, int out_fp32, void *out, kvq_stream_t stream) {
+    kvq_range r;
+    const int st = single_range(k_codes, v_codes, k_scales, v_scales, n_kv, &r);
+    if (st) return st;
+    return attention_common(q, n_q, &r, 1, hidden, group, sm_scale, out_fp32, out, stream, 1, q_pos0);
 }
 
 int kvq_device_status(kvq_stream_t stream) {

@@ -108,6 +108,8 @@ struct AttnParams {
     void *out;
     RangeTable ranges;
     int tiles_before[KVQ_MAX_RANGES + 1];
+    int causal;      // 1: query row i (at key position q_pos0 + i) sees keys j <= q_pos0 + i
+    int64_t q_pos0;  // single store only
 };
 
 // Staging buffers of packed codes, filled by bulk copies: two 16 KB stages.
@@ -408,6 +410,24 @@ __device__ __forceinline__ bool decode_tile(const uint8_t *stg_k, const uint8_t 
     return v_free || __all_sync(0xffffffffu, mbar_wait(v_empty, ph, abort_flag, &g_err_attn));
 }
 
+// First query row of this CTA.  Causal: CTA pairs in reverse order, the longest
+// first.  Recomputed where needed (from special registers) rather than kept live.
+template <bool CAUSAL>
+__device__ __forceinline__ int64_t cta_row0() {
+    const int64_t x = blockIdx.x;
+    return CAUSAL ? (static_cast<int64_t>(gridDim.x) - 2 - (x & ~int64_t(1)) + (x & 1)) * BQ : x * BQ;
+}
+// Key tiles this CTA pair walks: all of them, or (causal) those up to the
+// position of the pair's last query row; both CTAs of a pair get the same count.
+template <bool CAUSAL>
+__device__ __forceinline__ int cta_tiles(const AttnParams &p) {
+    if (!CAUSAL) return p.total_tiles;
+    const int64_t first = cta_row0<true>() & ~int64_t(2 * BQ - 1);  // the pair's first row
+    const int64_t end = p.n_q < first + 2 * BQ ? p.n_q : first + 2 * BQ;
+    const int64_t need = (p.q_pos0 + end - 1) / BKV + 1;
+    return need < p.total_tiles ? static_cast<int>(need) : p.total_tiles;
+}
+
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
     tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
     tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
@@ -416,7 +436,7 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
     tmem_ld_wait();
 }
 
-template <int GROUP, bool MIXED>
+template <int GROUP, bool MIXED, bool CAUSAL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ AttnParams p) {
     using L = SmemLayout;
@@ -450,8 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int head = blockIdx.y;
-    const int64_t q0 = static_cast<int64_t>(blockIdx.x) * BQ;
-    const int T = p.total_tiles;
+    const int T = cta_tiles<CAUSAL>(p);
 
     if (threadIdx.x == 0) {
         mbar_init(q_tma, 1);
@@ -495,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 mbar_arrive_expect_tx(q_tma, NQT * Q_TILE_BYTES);
 #pragma unroll
                 for (int t = 0; t < NQT; ++t) {
-                    const int y = static_cast<int>(q0) + t * BQT;
+                    const int y = static_cast<int>(cta_row0<CAUSAL>()) + t * BQT;
                     tma_load_2d(sQ + t * Q_TILE_BYTES, &tm_q, q_tma, head * 128, y);
                     tma_load_2d(sQ + t * Q_TILE_BYTES + Q_HALF_BYTES, &tm_q, q_tma, head * 128 + 64, y);
                 }
@@ -708,11 +727,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             uint32_t sr[128];
             tmem_ld128(sa, sr);
-            const int valid = cur.ref(p).valid;
-            if (valid < BKV) {
+            int nvis = cur.ref(p).valid;  // keys of this tile the row sees
+            if constexpr (CAUSAL) {
+                const int64_t lim = p.q_pos0 + cta_row0<true>() + t * BQT + r - static_cast<int64_t>(j) * BKV + 1;
+                if (lim < nvis) nvis = lim < 0 ? 0 : static_cast<int>(lim);
+            }
+            if (nvis < BKV) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+                    if (c >= nvis) sr[c] = __float_as_uint(-INFINITY);
             }
             float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
 #pragma unroll
@@ -805,7 +828,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             rotate128_thread(o);
-            const int64_t row = q0 + t * BQT + r;
+            const int64_t row = cta_row0<CAUSAL>() + t * BQT + r;
             if (row < p.n_q) {
                 if (p.out_fp32) {
                     float4 *dst =
@@ -839,10 +862,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_MMA) tmem_dealloc_pair(tmem, 512);
 }
 
-template <int GROUP, bool MIXED>
+template <int GROUP, bool MIXED, bool CAUSAL>
 int launch_one(const CUtensorMap &tm, const AttnParams &p, dim3 grid, cudaStream_t s) {
     constexpr int smem = SmemLayout::BYTES;
-    auto fn = attention_kernel<GROUP, MIXED>;
+    auto fn = attention_kernel<GROUP, MIXED, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) {
         fn<<<grid, NUM_THREADS, smem, s>>>(tm, p);
@@ -853,13 +876,14 @@ int launch_one(const CUtensorMap &tm, const AttnParams &p, dim3 grid, cudaStream
 
 template <int GROUP>
 int launch_group(const CUtensorMap &tm, const AttnParams &p, dim3 grid, bool mixed, cudaStream_t s) {
-    return mixed ? launch_one<GROUP, true>(tm, p, grid, s) : launch_one<GROUP, false>(tm, p, grid, s);
+    if (p.causal) return launch_one<GROUP, false, true>(tm, p, grid, s);  // single INT4 store
+    return mixed ? launch_one<GROUP, true, false>(tm, p, grid, s) : launch_one<GROUP, false, false>(tm, p, grid, s);
 }
 
 }  // namespace
 
 int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int hidden, int group, float sm_scale,
-                     int out_fp32, void *out, cudaStream_t s) {
+                     int out_fp32, void *out, cudaStream_t s, int causal, int64_t q_pos0) {
     alignas(64) CUtensorMap tm_q;
     if (encode_tmap_2d(&tm_q, q, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(n_q),
                        static_cast<uint64_t>(hidden) * 2, 64, BQT))
@@ -880,6 +904,8 @@ int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int h
     }
     p.tiles_before[ranges.n] = tiles;
     p.total_tiles = tiles;
+    p.causal = causal;
+    p.q_pos0 = q_pos0;
     // CTA pairs: an even number of CTAs of BQ query rows each
     const int64_t pairs = (n_q + 2 * BQ - 1) / (2 * BQ);
     dim3 grid(static_cast<unsigned>(2 * pairs), static_cast<unsigned>(hidden / 128));

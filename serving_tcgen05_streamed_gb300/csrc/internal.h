@@ -34,7 +34,7 @@ int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int gro
                     const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, const RangeTable &ranges,
                     cudaStream_t s);
 int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int hidden, int group, float sm_scale,
-                     int out_fp32, void *out, cudaStream_t s);
+                     int out_fp32, void *out, cudaStream_t s, int causal = 0, int64_t q_pos0 = 0);
 cudaError_t launch_selftest_wait(uint64_t ns, cudaStream_t s);
 
 // Device error words, one per translation unit: read-and-clear (synchronous).

@@ -96,6 +96,13 @@ def test_argument_errors_are_reported_before_any_launch():
     assert lib.packed_kv_attention(a16, 10, a16, a16, a16, a16, 5, 1024, 32, 0.0, 2, a16, S) == kvq.KVQ_ERR_ARG
     assert lib.packed_kv_attention(a16, 10, a16, a16, a16, a16, 5, 1024, 32, 0.0, 1, a16, S) == kvq.KVQ_ERR_ARG
     assert lib.packed_kv_attention(a16, 10, a16, odd, a16, a16, 5, 1024, 32, 0.0, 0, a16, S) == kvq.KVQ_ERR_ALIGN
+    # causal: a negative query position, and the checks it shares
+    assert lib.packed_kv_attention_causal(a16, 10, -1, a16, a16, a16, a16, 5, 1024, 32, 0.0, 0, a16, S) \
+        == kvq.KVQ_ERR_ARG
+    assert lib.packed_kv_attention_causal(a16, 10, 0, a16, a16, a16, a16, 0, 1024, 32, 0.0, 0, a16, S) \
+        == kvq.KVQ_ERR_ARG
+    assert lib.packed_kv_attention_causal(a16, 10, 0, a16, odd, a16, a16, 5, 1024, 32, 0.0, 0, a16, S) \
+        == kvq.KVQ_ERR_ALIGN
     # mixed range tables: gaps, bad bits, capacity
     R = _lib._Range
     bad_gap = (R * 2)(R(0, 100, 128, 4, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20),
