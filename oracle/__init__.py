@@ -68,7 +68,7 @@ def _load():
             lib.kvqo_kv_unpack.restype = I
             lib.kvqo_kv_unpack.argtypes = [P, P, P, P, I64, I, I, I, P]
             lib.kvqo_qkv_proj.restype = I
-            lib.kvqo_qkv_proj.argtypes = [P, P, I, P, I64, I, I, P, P, F, P, P, P, P, P, P]
+            lib.kvqo_qkv_proj.argtypes = [P, P, I, P, I64, I, I, P, P, F, P, I, P, P, P, P, P, P]
             lib.kvqo_attention.restype = I
             lib.kvqo_attention.argtypes = [P, I64, I, P, P, P, P, I64, I64, I, I, F, P, I64, P]
             lib.kvqo_attention_causal.restype = I
@@ -183,10 +183,13 @@ def kv_unpack(kc, vc, ks, vs, *, group: int = 32, bits: int = 4) -> np.ndarray:
 
 
 # ----------------------------------------------------------------- a2
-def qkv_proj(x, w, rows=None, *, group: int = 32, bits: int = 4, q_norm_w=None, k_norm_w=None, eps: float = 1e-6):
+def qkv_proj(x, w, rows=None, *, group: int = 32, bits: int = 4, q_norm_w=None, k_norm_w=None, eps: float = 1e-6,
+             rope_cs=None):
     """x: uint16 BF16 bits [n, C]; w: uint16 BF16 bits [3C, C].  Returns a dict
     with q_f32 [n_rows, C], q_bf16 [n_rows, C] (uint16) and compact
-    token-major k_codes, v_codes, k_scales, v_scales for `rows`."""
+    token-major k_codes, v_codes, k_scales, v_scales for `rows`.  rope_cs:
+    optional fp32 [n, rot_dim/2, 2] (cos, sin) per token row for the
+    split-half RoPE of Q and K after the RMSNorm."""
     x, w = _c(x, np.uint16), _c(w, np.uint16)
     n, C = x.shape
     assert w.shape == (3 * C, C)
@@ -194,6 +197,9 @@ def qkv_proj(x, w, rows=None, *, group: int = 32, bits: int = 4, q_norm_w=None, 
     heads = C // HD
     qn = None if q_norm_w is None else _c(q_norm_w, np.float32)
     kn = None if k_norm_w is None else _c(k_norm_w, np.float32)
+    rc_ = None if rope_cs is None else _c(rope_cs, np.float32)
+    rot = 0 if rc_ is None else 2 * rc_.shape[1]
+    assert rc_ is None or (rc_.shape[0] == n and rc_.shape[2] == 2)
     out = dict(
         q_f32=np.empty((len(rows), C), np.float32),
         q_bf16=np.empty((len(rows), C), np.uint16),
@@ -202,7 +208,7 @@ def qkv_proj(x, w, rows=None, *, group: int = 32, bits: int = 4, q_norm_w=None, 
         k_scales=np.empty((len(rows), heads, HD // group), np.uint16),
         v_scales=np.empty((len(rows), heads, HD // group), np.uint16),
     )
-    rc = _load().kvqo_qkv_proj(_p(x), _p(w), C, _p(rows), len(rows), group, bits, _p(qn), _p(kn), eps,
+    rc = _load().kvqo_qkv_proj(_p(x), _p(w), C, _p(rows), len(rows), group, bits, _p(qn), _p(kn), eps, _p(rc_), rot,
                                _p(out["q_f32"]), _p(out["q_bf16"]), _p(out["k_codes"]), _p(out["v_codes"]),
                                _p(out["k_scales"]), _p(out["v_scales"]))
     if rc:

@@ -261,18 +261,38 @@ static void rmsnorm128(float *v, const float *w, float eps) {
     for (int i = 0; i < HD; ++i) v[i] = (float)((double)v[i] * r * (double)w[i]);
 }
 
+/* Split-half rotary position embedding of one head vector, in place
+ * ([V] `_norm_rope`: "fused RMSNorm + split-half RoPE", rot_dim = twice the
+ * table's frequency count; the table itself is the caller's).  With h =
+ * rot_dim/2 and (c_i, s_i) = cs[2i], cs[2i+1] for i < h:
+ *   y_i     = x_i c_i - x_{i+h} s_i
+ *   y_{i+h} = x_{i+h} c_i + x_i s_i
+ * dims >= rot_dim unchanged; fp64 products and sum, rounded to fp32. */
+static void rope_split_half(float *v, const float *cs, int rot_dim) {
+    const int h = rot_dim / 2;
+    for (int i = 0; i < h; ++i) {
+        const double c = cs[2 * i], sn = cs[2 * i + 1], a = v[i], b = v[i + h];
+        v[i] = (float)(a * c - b * sn);
+        v[i + h] = (float)(b * c + a * sn);
+    }
+}
+
 /* For each listed token row t: acc = x[t] . W^T ([I] "Proposed backend
  * capability": the fused QKV GEMM), accumulated in fp64 and rounded to fp32.
  * Columns [0,C) are Q, [C,2C) K, [2C,3C) V, head h = 128 columns from h*128.
- * Q: optional RMSNorm (q_norm_w[128], may be NULL) -> rotate -> q_f32 and its
- * BF16 rounding q_bf16.  K: optional RMSNorm (k_norm_w) -> rotate -> quantise.
+ * Q: optional RMSNorm (q_norm_w[128], may be NULL) -> optional split-half
+ * RoPE (rope_cs: rot_dim floats per token row, (cos, sin) pairs, row t at
+ * rope_cs + t*rot_dim; NULL = none) -> rotate -> q_f32 and its BF16 rounding
+ * q_bf16.  K: optional RMSNorm (k_norm_w) -> optional RoPE -> rotate -> quantise.
  * V: rotate -> quantise.  The rotation and quantiser take the fp32
  * accumulator, with no BF16 rounding in between.  Outputs compact token-major
  * as in kvqo_kv_rotate_quant_pack; q_f32 / q_bf16 are [n_rows][C]. */
 int kvqo_qkv_proj(const uint16_t *x, const uint16_t *w, int hidden, const int64_t *rows, int64_t n_rows, int group,
-                  int bits, const float *q_norm_w, const float *k_norm_w, float eps, float *q_f32, uint16_t *q_bf16,
-                  uint8_t *k_codes, uint8_t *v_codes, uint16_t *k_scales, uint16_t *v_scales) {
+                  int bits, const float *q_norm_w, const float *k_norm_w, float eps, const float *rope_cs, int rot_dim,
+                  float *q_f32, uint16_t *q_bf16, uint8_t *k_codes, uint8_t *v_codes, uint16_t *k_scales,
+                  uint16_t *v_scales) {
     if (check_fmt(hidden, group, bits)) return 1;
+    if (rope_cs && (rot_dim < 2 || rot_dim > HD || rot_dim % 2)) return 1;
     const int C = hidden, heads = C / HD, cb = HD * bits / 8, sg = HD / group;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < n_rows; ++r) {
@@ -290,12 +310,14 @@ int kvqo_qkv_proj(const uint16_t *x, const uint16_t *w, int hidden, const int64_
         for (int h = 0; h < heads; ++h) {
             float *q = acc + h * HD, *kk = acc + C + h * HD, *vv = acc + 2 * C + h * HD;
             if (q_norm_w) rmsnorm128(q, q_norm_w, eps);
+            if (rope_cs) rope_split_half(q, rope_cs + rows[r] * rot_dim, rot_dim);
             kvqo_rotate128(q, y);
             for (int i = 0; i < HD; ++i) {
                 if (q_f32) q_f32[r * C + h * HD + i] = y[i];
                 if (q_bf16) q_bf16[r * C + h * HD + i] = kvqo_f32_to_bf16(y[i]);
             }
             if (k_norm_w) rmsnorm128(kk, k_norm_w, eps);
+            if (rope_cs) rope_split_half(kk, rope_cs + rows[r] * rot_dim, rot_dim);
             kvqo_rotate128(kk, y);
             kvqo_quant_head(y, group, bits, k_codes + (r * heads + h) * cb, k_scales + (r * heads + h) * sg);
             kvqo_rotate128(vv, y);

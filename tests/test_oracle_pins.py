@@ -287,6 +287,67 @@ def test_qkv_projection_rmsnorm_properties():
     assert abs(np.sqrt(np.mean(kq.astype(np.float64) ** 2)) - 1.0) < 0.1
 
 
+# ------------------------------------------------------------------ split-half RoPE in the projection (next row f2)
+def _rope_table(n, rot_dim, base=10000.0, pos=None):
+    """Standard rotary table: angle pos * base^(-2i/rot_dim) for frequency i."""
+    pos = np.arange(n, dtype=np.float64) if pos is None else np.asarray(pos, np.float64)
+    freq = base ** (-2.0 * np.arange(rot_dim // 2) / rot_dim)
+    ang = pos[:, None] * freq[None, :]
+    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+
+
+def _proj_inputs(n=6, C=256, seed=31):
+    r = _rng(seed)
+    x = _bf16_bits(torch.from_numpy(r.standard_normal((n, C)).astype(np.float32)).to(torch.bfloat16))
+    w = _bf16_bits(torch.from_numpy((r.standard_normal((3 * C, C)) * C ** -0.5).astype(np.float32)).to(torch.bfloat16))
+    return x, w
+
+
+def test_rope_identity_table_changes_nothing():
+    x, w = _proj_inputs()
+    cs = np.zeros((x.shape[0], 64, 2), np.float32)
+    cs[..., 0] = 1.0
+    a = oracle.qkv_proj(x, w)
+    b = oracle.qkv_proj(x, w, rope_cs=cs)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("rot_dim", [128, 64])
+def test_rope_quarter_turn_moves_the_second_half_with_a_minus_sign(rot_dim):
+    # cos 0, sin 1: y_i = -x_{i+h}, y_{i+h} = x_i for i < h = rot_dim/2; dims past rot_dim unchanged
+    x, w = _proj_inputs()
+    n, C = x.shape
+    cs = np.zeros((n, rot_dim // 2, 2), np.float32)
+    cs[..., 1] = 1.0
+    u0 = oracle.qkv_proj(x, w)["q_f32"].reshape(n, C // HD, HD).astype(np.float64) @ H
+    u1 = oracle.qkv_proj(x, w, rope_cs=cs)["q_f32"].reshape(n, C // HD, HD).astype(np.float64) @ H
+    h = rot_dim // 2
+    exp = u0.copy()
+    exp[..., :h] = -u0[..., h:rot_dim]
+    exp[..., h:rot_dim] = u0[..., :h]
+    assert np.allclose(u1, exp, atol=1e-5)
+
+
+def test_rope_keeps_norms_and_dot_products_depend_on_position_difference():
+    # the same token at every position: |q| unchanged, and q_m . q_n depends on m - n only
+    x, w = _proj_inputs(n=1)
+    n = 12
+    xs = np.repeat(x, n, axis=0)
+    cs = _rope_table(n, 128)
+    q0 = oracle.qkv_proj(xs, w)["q_f32"].astype(np.float64)
+    q1 = oracle.qkv_proj(xs, w, rope_cs=cs)["q_f32"].astype(np.float64)
+    heads = x.shape[1] // HD
+    q0 = q0.reshape(n, heads, HD)
+    q1 = q1.reshape(n, heads, HD)
+    assert np.allclose(np.linalg.norm(q1, axis=-1), np.linalg.norm(q0, axis=-1), rtol=1e-5)
+    for d in (1, 3, 5):
+        dots = np.array([np.sum(q1[m] * q1[m + d], axis=-1) for m in range(n - d)])
+        assert np.allclose(dots, dots[0], rtol=1e-4, atol=1e-4)
+    # and it is not the identity: neighbouring positions differ
+    assert not np.allclose(q1[1], q1[0], atol=1e-3)
+
+
 # ------------------------------------------------------------------ a4 attention
 def _head_major(kc, vc, ks, vs, n_pad):
     """compact token-major [n, heads, ...] -> head-major [heads, n_pad, ...] with zero pad rows."""
