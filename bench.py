@@ -260,7 +260,12 @@ def run_gpu(args, wl, world, rank, local):
     if world > 1:  # independent problems per rank
         x = x.roll(rank * 7, dims=0)
     causal = args.workload == "causal"
-    wl_label = wl.name + (", causal attention" if causal else "")
+    wl_label = wl.name + (", causal attention" if causal else "") + (", RoPE 128 in the projection" if args.rope else "")
+    rope = None
+    if args.rope:  # split-half RoPE table of Q and K: token position t, frequencies 10000^(-2i/128)
+        pos = torch.arange(n, dtype=torch.float64, device=dev)[:, None]
+        ang = pos * (10000.0 ** (-2.0 * torch.arange(64, dtype=torch.float64, device=dev) / 128))[None, :]
+        rope = torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).to(torch.float32).contiguous()
     fp, fa = flops(n, C, causal)
 
     mixed = wl is inputs.MIXED
@@ -274,7 +279,10 @@ def run_gpu(args, wl, world, rank, local):
     q = torch.empty((n, C), dtype=torch.bfloat16, device=dev)
 
     def project(xin):
-        if mixed:
+        if rope is not None:
+            kvq.streamed_qkv_proj_rope(xin, w, stores, rope, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
+                                       k_norm_w=kn, q_out=q, stream=stream)
+        elif mixed:
             kvq.streamed_qkv_proj_mixed(xin, w, stores, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
                                         k_norm_w=kn, q_out=q, stream=stream)
         else:
@@ -355,8 +363,14 @@ def run_gpu(args, wl, world, rank, local):
                 landed.append(ev)
         for (s0, ln), ev in zip(in_chunks, landed):
             stream.wait_event(ev)
-            kvq.streamed_qkv_proj_mixed(x_dev[s0:s0 + ln], w, windows(s0, ln), group=32, chunk_tokens=wl.chunk_tokens,
-                                        q_norm_w=qn, k_norm_w=kn, q_out=q[s0:s0 + ln], stream=stream)
+            if rope is not None:
+                kvq.streamed_qkv_proj_rope(x_dev[s0:s0 + ln], w, windows(s0, ln), rope[s0:s0 + ln], group=32,
+                                           chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q[s0:s0 + ln],
+                                           stream=stream)
+            else:
+                kvq.streamed_qkv_proj_mixed(x_dev[s0:s0 + ln], w, windows(s0, ln), group=32,
+                                            chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn,
+                                            q_out=q[s0:s0 + ln], stream=stream)
         for s0, ln in out_chunks:
             qc = q[s0:s0 + ln]
             if mixed:
@@ -401,7 +415,7 @@ def run_gpu(args, wl, world, rank, local):
                 traffic = rec.get("bytes_per_launch")
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not mixed and not causal:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not mixed and not causal and rope is None:
         del x_host, out_host, x_dev
         sample = CpuOracleSample(wl, seed=7, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
         t_block = sample.run()
@@ -415,7 +429,7 @@ def run_gpu(args, wl, world, rank, local):
             "vs_baseline": None, "dtype": "bf16 GEMM / fp16 attention operands, fp32 accumulate",
             "data": "synthetic (seeded generators; random-init weights of the H3 block shape)",
             "config": {"workload": wl_label, "n_tokens": n, "hidden": C,
-                       "heads": wl.heads, "group": 32, "causal": causal,
+                       "heads": wl.heads, "group": 32, "causal": causal, "rope": rope is not None,
                        "kv_bits": "8/4 by token range" if mixed else 4, "chunk_tokens": wl.chunk_tokens,
                        "qk_rmsnorm": True,
                        "l2": f"inputs larger than L2 (x {n * C * 2 / GiB:.2f} GiB, packed K/V "
@@ -512,6 +526,8 @@ def main():
                     help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling); "
                          "mixed: N=217,088 with INT8 conditioning ranges; causal: the N=152,263 block with causal "
                          "attention; sweep: pack/unpack bandwidth")
+    ap.add_argument("--rope", action="store_true",
+                    help="split-half RoPE (rot_dim 128) of Q and K in the projection epilogue")
     ap.add_argument("--sweep-n", type=int, nargs="+", default=None,
                     help="sweep: token counts to run (default: 4,096 ... 262,144)")
     ap.add_argument("--sweep-groups", type=int, nargs="+", default=None, choices=(32, 64, 128),

@@ -183,6 +183,23 @@ KVQ_API int streamed_qkv_proj_mixed(const void *x, const void *w_qkv, int64_t n,
                             int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
                             void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream);
 
+/* ---------------------------------------------------------------- next row f2: RoPE in the projection epilogue
+ * streamed_qkv_proj_mixed with a split-half rotary position embedding of Q and
+ * K, applied after the RMSNorm and before the Hadamard rotation (vram_lab.py
+ * `_norm_rope`: "fused RMSNorm + split-half RoPE").  rope_cs: fp32, rot_dim
+ * floats per token row of x, row t at rope_cs + t*rot_dim, holding the pairs
+ * (cos_i, sin_i), i < rot_dim/2; with H = rot_dim/2, dims i and i+H of each
+ * head become x_i cos_i - x_{i+H} sin_i and x_{i+H} cos_i + x_i sin_i, dims
+ * past rot_dim stay.  The table is the caller's (positions and frequencies
+ * are not the library's business); it is read, 16-byte aligned, owned by the
+ * caller.  rot_dim 64 or 128, else KVQ_ERR_UNSUPPORTED; rope_cs == NULL means
+ * no RoPE (then this is streamed_qkv_proj_mixed).  Other arguments and errors
+ * as streamed_qkv_proj_mixed. */
+KVQ_API int streamed_qkv_proj_rope(const void *x, const void *w_qkv, int64_t n, int hidden, int group,
+                           int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
+                           const float *rope_cs, int rot_dim, void *q_out, const kvq_range *ranges, int n_ranges,
+                           kvq_stream_t stream);
+
 KVQ_API int packed_kv_attention_mixed(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges, int hidden,
                               int group, float sm_scale, int out_fp32, void *out, kvq_stream_t stream);
 

@@ -201,6 +201,15 @@ int kv_unpack(const void *k_codes, const void *v_codes, const void *k_scales, co
 int streamed_qkv_proj_mixed(const void *x, const void *w_qkv, int64_t n, int hidden, int group,
                             int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
                             void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream) {
+    return streamed_qkv_proj_rope(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps, nullptr, 0,
+                                  q_out, ranges, n_ranges, stream);
+}
+
+int streamed_qkv_proj_rope(const void *x, const void *w_qkv, int64_t n, int hidden, int group, int64_t chunk_tokens,
+                           const float *q_norm_w, const float *k_norm_w, float eps, const float *rope_cs,
+                           int rot_dim, void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream) {
+    if (rope_cs && rot_dim != 64 && rot_dim != 128) return KVQ_ERR_UNSUPPORTED;
+    if (rope_cs && !aligned16(rope_cs)) return KVQ_ERR_ALIGN;
     if (!x || !w_qkv || !q_out) return KVQ_ERR_ARG;
     if (n < 1 || n > (int64_t(1) << 31) - 256 || !valid_hidden(hidden) || !valid_group(group) || chunk_tokens < 0)
         return KVQ_ERR_ARG;
@@ -214,7 +223,7 @@ int streamed_qkv_proj_mixed(const void *x, const void *w_qkv, int64_t n, int hid
     int st = check_range_table(ranges, n_ranges, n, hidden, group, true, &t);
     if (st) return st;
     return launch_qkv_proj(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps, q_out, t,
-                           reinterpret_cast<cudaStream_t>(stream));
+                           reinterpret_cast<cudaStream_t>(stream), rope_cs, rot_dim);
 }
 
 int streamed_qkv_proj(const void *x, const void *w_qkv, int64_t n, int hidden, int group, int64_t chunk_tokens,

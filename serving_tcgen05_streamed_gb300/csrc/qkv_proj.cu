@@ -55,6 +55,7 @@ struct ProjParams {
     const float *q_norm_w;
     const float *k_norm_w;
     float eps;
+    const float *rope_cs;  // split-half RoPE table, rot_dim floats ((cos, sin) pairs) per token row, or null
     __nv_bfloat16 *q_out;
     RangeTable ranges;
 };
@@ -84,6 +85,26 @@ __device__ __forceinline__ void rmsnorm128(float (&v)[128], const float *__restr
     for (int i = 0; i < 128; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], r), __ldg(w + i));
 }
 
+// Split-half rotary position embedding of one head row in registers (the
+// `_norm_rope` step of vram_lab.py: after the RMSNorm, before the Hadamard
+// rotation): with H = ROT/2 and (c_i, s_i) from the row's table,
+// y_i = x_i c_i - x_{i+H} s_i and y_{i+H} = x_{i+H} c_i + x_i s_i for i < H;
+// fp32 products, then one fp32 sum.
+template <int ROT>
+__device__ __forceinline__ void rope_split_half(float (&v)[128], const float *__restrict__ cs) {
+    constexpr int H = ROT / 2;
+    const float4 *t4 = reinterpret_cast<const float4 *>(cs);
+#pragma unroll
+    for (int i = 0; i < H; i += 2) {
+        const float4 t = __ldg(t4 + i / 2);  // c_i, s_i, c_{i+1}, s_{i+1}
+        const float a0 = v[i], b0 = v[i + H], a1 = v[i + 1], b1 = v[i + 1 + H];
+        v[i] = __fsub_rn(__fmul_rn(a0, t.x), __fmul_rn(b0, t.y));
+        v[i + H] = __fadd_rn(__fmul_rn(b0, t.x), __fmul_rn(a0, t.y));
+        v[i + 1] = __fsub_rn(__fmul_rn(a1, t.z), __fmul_rn(b1, t.w));
+        v[i + 1 + H] = __fadd_rn(__fmul_rn(b1, t.z), __fmul_rn(a1, t.w));
+    }
+}
+
 template <int GROUP, int BITS>
 __device__ __forceinline__ void store_codes(const float (&v)[128], uint8_t *codes_row, uint16_t *scales_row) {
     uint32_t words[128 * BITS / 32];
@@ -103,7 +124,7 @@ __device__ __forceinline__ void store_codes(const float (&v)[128], uint8_t *code
     }
 }
 
-template <int GROUP>
+template <int GROUP, int ROT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ ProjParams p) {
@@ -253,6 +274,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int head = (gcol - sect * C) >> 7;
                 if (sect == 0) {
                     if (p.q_norm_w) rmsnorm128(v, p.q_norm_w, p.eps);
+                    if constexpr (ROT > 0) {
+                        if (row < p.n) rope_split_half<ROT>(v, p.rope_cs + row * ROT);
+                    }
                     rotate128_thread(v);
                     if (row < p.n) {
                         uint4 *dst = reinterpret_cast<uint4 *>(p.q_out + row * C + head * 128);
@@ -269,6 +293,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else {
                     if (sect == 1 && p.k_norm_w) rmsnorm128(v, p.k_norm_w, p.eps);
+                    if constexpr (ROT > 0) {
+                        if (sect == 1 && row < p.n) rope_split_half<ROT>(v, p.rope_cs + row * ROT);
+                    }
                     rotate128_thread(v);
                     // the range holding this token (rows past n belong to the last range's padding)
                     int g = 0;
@@ -305,9 +332,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
+namespace {
+template <int GROUP, int ROT>
+cudaError_t launch_proj(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const ProjParams &p, int grid,
+                        cudaStream_t s) {
+    auto fn = qkv_proj_kernel<GROUP, ROT>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess) fn<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, p);
+    return e;
+}
+template <int GROUP>
+cudaError_t launch_rot(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const ProjParams &p, int rot, int grid,
+                       cudaStream_t s) {
+    if (rot == 64) return launch_proj<GROUP, 64>(tm_x, tm_w, p, grid, s);
+    if (rot == 128) return launch_proj<GROUP, 128>(tm_x, tm_w, p, grid, s);
+    return launch_proj<GROUP, 0>(tm_x, tm_w, p, grid, s);
+}
+}  // namespace
+
 int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int group, int64_t chunk_tokens,
                     const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, const RangeTable &ranges,
-                    cudaStream_t s) {
+                    cudaStream_t s, const float *rope_cs, int rot_dim) {
     alignas(64) CUtensorMap tm_x, tm_w;
     if (encode_tmap_2d(&tm_x, x, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(n),
                        static_cast<uint64_t>(hidden) * 2, BK, BM))
@@ -330,18 +375,13 @@ int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int gro
     p.eps = eps;
     p.q_out = static_cast<__nv_bfloat16 *>(q_out);
     p.ranges = ranges;
+    p.rope_cs = rope_cs;
+    const int rot = rope_cs ? rot_dim : 0;
     const int grid = static_cast<int>(p.total_tiles < sm_count() ? p.total_tiles : sm_count());
     cudaError_t e;
-    if (group == 32) {
-        e = cudaFuncSetAttribute(qkv_proj_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e == cudaSuccess) qkv_proj_kernel<32><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, p);
-    } else if (group == 64) {
-        e = cudaFuncSetAttribute(qkv_proj_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e == cudaSuccess) qkv_proj_kernel<64><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, p);
-    } else {
-        e = cudaFuncSetAttribute(qkv_proj_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e == cudaSuccess) qkv_proj_kernel<128><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w, p);
-    }
+    if (group == 32) e = launch_rot<32>(tm_x, tm_w, p, rot, grid, s);
+    else if (group == 64) e = launch_rot<64>(tm_x, tm_w, p, rot, grid, s);
+    else e = launch_rot<128>(tm_x, tm_w, p, rot, grid, s);
     if (e == cudaSuccess) e = cudaGetLastError();
     return report_cuda(e, "projection launch");
 }
