@@ -280,7 +280,7 @@ def run_gpu(args, wl, world, rank, local):
 
     def project(xin):
         if rope is not None:
-            kvq.streamed_qkv_proj_rope(xin, w, stores, rope, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
+            kvq.streamed_qkv_proj_ex(xin, w, stores, rope, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
                                        k_norm_w=kn, q_out=q, stream=stream)
         elif mixed:
             kvq.streamed_qkv_proj_mixed(xin, w, stores, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
@@ -364,7 +364,7 @@ def run_gpu(args, wl, world, rank, local):
         for (s0, ln), ev in zip(in_chunks, landed):
             stream.wait_event(ev)
             if rope is not None:
-                kvq.streamed_qkv_proj_rope(x_dev[s0:s0 + ln], w, windows(s0, ln), rope[s0:s0 + ln], group=32,
+                kvq.streamed_qkv_proj_ex(x_dev[s0:s0 + ln], w, windows(s0, ln), rope[s0:s0 + ln], group=32,
                                            chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q[s0:s0 + ln],
                                            stream=stream)
             else:
@@ -396,6 +396,76 @@ def run_gpu(args, wl, world, rank, local):
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     e2e_s = max_over_ranks(world, e2e_s)
     e2e_val = world * (fp + fa) / e2e_s / 1e12
+
+    # ------------------------------------------------------------ end to end, two phases (no full Q or output on device)
+    # Phase 1 projects K/V only, by token chunks of x landing from the host; phase 2
+    # brings x in again by query chunks, recomputes their Q only and attends, each
+    # output chunk going back to the host.  Device memory: W, the packed store and
+    # two chunk buffers of each kind.  Same FLOPs as the one-call path (the
+    # projection's sections split its columns).
+    del x_dev
+    torch.cuda.synchronize()
+    mem0 = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    xb = [torch.empty((E2E_IN_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    xq = [torch.empty((E2E_OUT_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    qb = [torch.empty((E2E_OUT_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in1", "p1", "in2", "qp", "attn", "out")}
+
+    def e2e_two_phase_step():
+        for i, (s0, ln) in enumerate(in_chunks):
+            b = i % 2
+            copy.wait_event(ev["p1"][b])  # chunk i-2's projection has read xb[b]
+            with torch.cuda.stream(copy):
+                xb[b][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+            ev["in1"][b].record(copy)
+            stream.wait_event(ev["in1"][b])
+            kvq.streamed_qkv_proj_ex(xb[b][:ln], w, windows(s0, ln), rope[s0:s0 + ln] if rope is not None else None,
+                                     sections=kvq.SECTION_KV, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
+                                     k_norm_w=kn, stream=stream)
+            ev["p1"][b].record(stream)
+        for i, (s0, ln) in enumerate(out_chunks):
+            b = i % 2
+            if i == 0:
+                with torch.cuda.stream(copy):
+                    xq[0][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+                ev["in2"][0].record(copy)
+            stream.wait_event(ev["in2"][b])
+            stream.wait_event(ev["out"][b])  # chunk i-2's output has left qb[b]
+            qc = kvq.streamed_qkv_proj_ex(xq[b][:ln], w, None, rope[s0:s0 + ln] if rope is not None else None,
+                                          sections=kvq.SECTION_Q, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
+                                          k_norm_w=kn, q_out=qb[b][:ln], stream=stream)
+            ev["qp"][b].record(stream)
+            if mixed:
+                kvq.packed_kv_attention_mixed(qc, stores, out=qc, stream=stream)
+            elif causal:
+                kvq.packed_kv_attention_causal(qc, store, q_pos0=s0, out=qc, stream=stream)
+            else:
+                kvq.packed_kv_attention(qc, store, out=qc, stream=stream)
+            ev["attn"][b].record(stream)
+            if i + 1 < len(out_chunks):  # next chunk's x, once the projection of chunk i-1 has read xq[1-b]
+                s1, l1 = out_chunks[i + 1]
+                copy.wait_event(ev["qp"][1 - b])
+                with torch.cuda.stream(copy):
+                    xq[1 - b][:l1].copy_(x_host[s1:s1 + l1], non_blocking=True)
+                ev["in2"][1 - b].record(copy)
+            copy.wait_event(ev["attn"][b])
+            with torch.cuda.stream(copy):
+                out_host[s0:s0 + ln].copy_(qc, non_blocking=True)
+            ev["out"][b].record(copy)
+        torch.cuda.synchronize()
+
+    for i in range(1 + e2e_steps):
+        if i == 1:
+            torch.cuda.synchronize()
+            barrier(world)
+            t0 = time.perf_counter()
+        e2e_two_phase_step()
+    e2e2_s = max_over_ranks(world, (time.perf_counter() - t0) / e2e_steps)
+    peak2_gib = (torch.cuda.max_memory_allocated(dev) - mem0) / GiB
+    # device memory the step holds beyond what stays resident across steps (W, norms, table)
+    resident_gib = (sum(st_.nbytes() for st_ in stores)) / GiB
+    assert kvq.device_status() == kvq.KVQ_OK
 
     # ------------------------------------------------------------ roofline of the dominant kernel (attention)
     peaks, peak_kind = load_peaks()
@@ -451,6 +521,15 @@ def run_gpu(args, wl, world, rank, local):
                     "note": "x copied in from pinned host memory and the attention output copied back each step, "
                             "on a copy stream overlapping the kernels (token chunks in, query chunks out); "
                             "W stays resident"},
+            "e2e_two_phase": {"value": world * (fp + fa) / e2e2_s / 1e12, "unit": "TFLOP/s",
+                              "ms_per_step": e2e2_s * 1e3,
+                              "device_gib": resident_gib + peak2_gib,
+                              "device_gib_materialise_bf16_qkv": peak_mat,
+                              "h2d_bytes_per_step": int(2 * x.numel() * 2), "d2h_bytes_per_step": int(n * C * 2),
+                              "note": "phase 1: K/V only by token chunks of x from the host; phase 2: x again by "
+                                      "query chunks, Q only recomputed, attention, output chunk back to the host; "
+                                      "device_gib = packed store + chunk buffers (x, Q and output never held in "
+                                      "full), W excluded as in the peak comparison"},
             "gpu_launches": 2 * args.steps,
             "cpu_baseline": cpu,
         }

@@ -122,6 +122,7 @@ KVQ_API int kv_unpack(const void *k_codes, const void *v_codes, const void *k_sc
  * the fp32 accumulator directly.  Tokens are processed chunk by chunk in
  * chunk_tokens-row chunks (0 = one chunk); results do not depend on the
  * chunk size.  No [n][3*hidden] tensor and no BF16 K/V exist at any time.
+ * The stores' pad rows n .. kvq_padded_rows(n)-1 are set to zero.
  * q_out must not alias x. */
 KVQ_API int streamed_qkv_proj(const void *x, const void *w_qkv, int64_t n, int hidden, int group, int64_t chunk_tokens,
                       const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, void *k_codes,
@@ -162,11 +163,10 @@ KVQ_API int packed_kv_attention_causal(const void *q, int64_t n_q, int64_t q_pos
  * of its arrays); token t of the sequence is row t - start of the range that
  * holds it.  Ranges must be given in order and tile [0, n) exactly, at most
  * KVQ_MAX_RANGES of them.  INT8 ranges use the same rotation, so Q and the
- * output need no per-range handling.  The projection also writes the rows
- * of the last range from len up to the next multiple of 128 (the codes of
- * zero rows); no other row past len is touched, so a range may be a window
- * (pointers advanced by the window's first row, cap the store's head stride)
- * into a larger store. */
+ * output need no per-range handling.  The projection writes rows 0 .. len-1
+ * of every range and nothing past them (the attention never reads rows past
+ * len as keys), so a range may be a window into a larger store: pointers
+ * advanced by the window's first row, cap the store's head stride. */
 typedef struct kvq_range {
     int64_t start;
     int64_t len;
@@ -183,22 +183,33 @@ KVQ_API int streamed_qkv_proj_mixed(const void *x, const void *w_qkv, int64_t n,
                             int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
                             void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream);
 
-/* ---------------------------------------------------------------- next row f2: RoPE in the projection epilogue
- * streamed_qkv_proj_mixed with a split-half rotary position embedding of Q and
- * K, applied after the RMSNorm and before the Hadamard rotation (vram_lab.py
- * `_norm_rope`: "fused RMSNorm + split-half RoPE").  rope_cs: fp32, rot_dim
- * floats per token row of x, row t at rope_cs + t*rot_dim, holding the pairs
- * (cos_i, sin_i), i < rot_dim/2; with H = rot_dim/2, dims i and i+H of each
- * head become x_i cos_i - x_{i+H} sin_i and x_{i+H} cos_i + x_i sin_i, dims
- * past rot_dim stay.  The table is the caller's (positions and frequencies
- * are not the library's business); it is read, 16-byte aligned, owned by the
- * caller.  rot_dim 64 or 128, else KVQ_ERR_UNSUPPORTED; rope_cs == NULL means
- * no RoPE (then this is streamed_qkv_proj_mixed).  Other arguments and errors
- * as streamed_qkv_proj_mixed. */
-KVQ_API int streamed_qkv_proj_rope(const void *x, const void *w_qkv, int64_t n, int hidden, int group,
-                           int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
-                           const float *rope_cs, int rot_dim, void *q_out, const kvq_range *ranges, int n_ranges,
-                           kvq_stream_t stream);
+/* ---------------------------------------------------------------- next rows f2, f3: RoPE, sections
+ * streamed_qkv_proj_mixed with two additions.
+ *
+ * RoPE (vram_lab.py `_norm_rope`: "fused RMSNorm + split-half RoPE"): a
+ * split-half rotary position embedding of Q and K, applied after the RMSNorm
+ * and before the Hadamard rotation.  rope_cs: fp32, rot_dim floats per token
+ * row of x, row t at rope_cs + t*rot_dim, holding the pairs (cos_i, sin_i),
+ * i < rot_dim/2; with H = rot_dim/2, dims i and i+H of each head become
+ * x_i cos_i - x_{i+H} sin_i and x_{i+H} cos_i + x_i sin_i, dims past rot_dim
+ * stay.  The table is the caller's (positions and frequencies are not the
+ * library's business), read only, 16-byte aligned.  rot_dim 64 or 128, else
+ * KVQ_ERR_UNSUPPORTED; rope_cs == NULL means no RoPE.
+ *
+ * Sections (vram_lab.py's two phases: K/V of every token first, then Q
+ * recomputed per query chunk): KVQ_SECTION_Q computes and writes Q only (the
+ * GEMM walks W's first hidden rows; ranges may be NULL), KVQ_SECTION_KV the K/V
+ * stores only (W's last 2*hidden rows; q_out may be NULL), both = the full
+ * projection.  Each section's bytes are those of the full call.
+ *
+ * Other arguments and errors as streamed_qkv_proj_mixed; KVQ_ERR_ARG for
+ * sections outside 1..3. */
+#define KVQ_SECTION_Q 1
+#define KVQ_SECTION_KV 2
+KVQ_API int streamed_qkv_proj_ex(const void *x, const void *w_qkv, int64_t n, int hidden, int group,
+                         int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
+                         const float *rope_cs, int rot_dim, int sections, void *q_out, const kvq_range *ranges,
+                         int n_ranges, kvq_stream_t stream);
 
 KVQ_API int packed_kv_attention_mixed(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges, int hidden,
                               int group, float sm_scale, int out_fp32, void *out, kvq_stream_t stream);

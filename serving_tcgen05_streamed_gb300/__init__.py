@@ -7,5 +7,5 @@ from ._lib import (  # noqa: F401
     EXPORTS, KVQ_ERR_ALIGN, KVQ_ERR_ARG, KVQ_ERR_CUDA, KVQ_ERR_TIMEOUT, KVQ_ERR_UNSUPPORTED, KVQ_OK, KvqError,
     PackedKV, codes_bytes, device_status, kv_rotate_quant_pack, kv_unpack, load, packed_kv_attention,
     packed_kv_attention_causal, packed_kv_attention_mixed, padded_rows, scales_bytes, selftest_wait_timeout, status_str,
-    streamed_qkv_proj, streamed_qkv_proj_mixed, streamed_qkv_proj_rope, version,
+    streamed_qkv_proj, streamed_qkv_proj_mixed, streamed_qkv_proj_ex, SECTION_Q, SECTION_KV, version,
 )

@@ -25,7 +25,7 @@ KVQ_OK, KVQ_ERR_ARG, KVQ_ERR_ALIGN, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_T
 EXPORTS = (
     "kvq_status_str", "kvq_version", "kvq_padded_rows", "kvq_codes_bytes", "kvq_scales_bytes",
     "kv_rotate_quant_pack", "kv_unpack", "streamed_qkv_proj", "packed_kv_attention",
-    "packed_kv_attention_causal", "streamed_qkv_proj_mixed", "streamed_qkv_proj_rope", "packed_kv_attention_mixed",
+    "packed_kv_attention_causal", "streamed_qkv_proj_mixed", "streamed_qkv_proj_ex", "packed_kv_attention_mixed",
     "kvq_device_status",
     "kvq_selftest_wait_timeout",
 )
@@ -83,8 +83,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.packed_kv_attention_causal.argtypes = [P, I64, I64, P, P, P, P, I64, I, I, F, I, P, P]
         lib.streamed_qkv_proj_mixed.restype = I
         lib.streamed_qkv_proj_mixed.argtypes = [P, P, I64, I, I, I64, P, P, F, P, ctypes.POINTER(_Range), I, P]
-        lib.streamed_qkv_proj_rope.restype = I
-        lib.streamed_qkv_proj_rope.argtypes = [P, P, I64, I, I, I64, P, P, F, P, I, P, ctypes.POINTER(_Range), I, P]
+        lib.streamed_qkv_proj_ex.restype = I
+        lib.streamed_qkv_proj_ex.argtypes = [P, P, I64, I, I, I64, P, P, F, P, I, I, P, ctypes.POINTER(_Range), I, P]
         lib.packed_kv_attention_mixed.restype = I
         lib.packed_kv_attention_mixed.argtypes = [P, I64, ctypes.POINTER(_Range), I, I, I, F, I, P, P]
         lib.kvq_device_status.restype = I
@@ -288,22 +288,34 @@ def streamed_qkv_proj_mixed(x: torch.Tensor, w_qkv: torch.Tensor, stores: list[P
     return q_out
 
 
-def streamed_qkv_proj_rope(x: torch.Tensor, w_qkv: torch.Tensor, stores: list[PackedKV], rope_cs: torch.Tensor,
-                           group: int = 32, chunk_tokens: int = 0, q_norm_w=None, k_norm_w=None, eps: float = 1e-6,
-                           q_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """streamed_qkv_proj_mixed with split-half RoPE of Q and K after the RMSNorm.
-    rope_cs: fp32 [n, rot_dim/2, 2] (cos, sin) per token row of x, rot_dim 64 or 128."""
+SECTION_Q, SECTION_KV = 1, 2
+
+
+def streamed_qkv_proj_ex(x: torch.Tensor, w_qkv: torch.Tensor, stores: list[PackedKV] | None = None,
+                         rope_cs: torch.Tensor | None = None, sections: int = SECTION_Q | SECTION_KV, group: int = 32,
+                         chunk_tokens: int = 0, q_norm_w=None, k_norm_w=None, eps: float = 1e-6,
+                         q_out: torch.Tensor | None = None, stream=None) -> torch.Tensor | None:
+    """streamed_qkv_proj_mixed with optional split-half RoPE of Q and K after the
+    RMSNorm (rope_cs: fp32 [n, rot_dim/2, 2] (cos, sin) per token row of x,
+    rot_dim 64 or 128) and a section mask: SECTION_Q writes Q only, SECTION_KV
+    the stores only.  Returns q_rot (None without SECTION_Q)."""
     _need_cuda(x, w_qkv, q_norm_w, k_norm_w, rope_cs)
     n, C = x.shape
-    assert rope_cs.dtype == torch.float32 and rope_cs.is_contiguous() and rope_cs.shape[0] == n
-    assert rope_cs.dim() == 3 and rope_cs.shape[2] == 2
-    q_out = torch.empty((n, C), dtype=torch.bfloat16, device=x.device) if q_out is None else q_out
-    arr = _ranges(stores)
-    st = load().streamed_qkv_proj_rope(_ptr(x), _ptr(w_qkv), n, C, group, chunk_tokens, _ptr(q_norm_w),
-                                       _ptr(k_norm_w), eps, _ptr(rope_cs), 2 * rope_cs.shape[1], _ptr(q_out), arr,
-                                       len(stores), _stream(stream))
-    _check(st, "streamed_qkv_proj_rope")
-    return q_out
+    want_q, want_kv = bool(sections & SECTION_Q), bool(sections & SECTION_KV)
+    if rope_cs is not None:
+        assert rope_cs.dtype == torch.float32 and rope_cs.is_contiguous() and rope_cs.shape[0] == n
+        assert rope_cs.dim() == 3 and rope_cs.shape[2] == 2
+    if want_q and q_out is None:
+        q_out = torch.empty((n, C), dtype=torch.bfloat16, device=x.device)
+    if want_kv:
+        arr, nr = _ranges(stores), len(stores)
+    else:
+        arr, nr = None, 0
+    st = load().streamed_qkv_proj_ex(_ptr(x), _ptr(w_qkv), n, C, group, chunk_tokens, _ptr(q_norm_w), _ptr(k_norm_w),
+                                     eps, _ptr(rope_cs), 0 if rope_cs is None else 2 * rope_cs.shape[1], sections,
+                                     _ptr(q_out) if want_q else None, arr, nr, _stream(stream))
+    _check(st, "streamed_qkv_proj_ex")
+    return q_out if want_q else None
 
 
 def packed_kv_attention_mixed(q: torch.Tensor, stores: list[PackedKV], sm_scale: float = 0.0,

@@ -201,29 +201,35 @@ int kv_unpack(const void *k_codes, const void *v_codes, const void *k_scales, co
 int streamed_qkv_proj_mixed(const void *x, const void *w_qkv, int64_t n, int hidden, int group,
                             int64_t chunk_tokens, const float *q_norm_w, const float *k_norm_w, float eps,
                             void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream) {
-    return streamed_qkv_proj_rope(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps, nullptr, 0,
-                                  q_out, ranges, n_ranges, stream);
+    return streamed_qkv_proj_ex(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps, nullptr, 0,
+                                KVQ_SECTION_Q | KVQ_SECTION_KV, q_out, ranges, n_ranges, stream);
 }
 
-int streamed_qkv_proj_rope(const void *x, const void *w_qkv, int64_t n, int hidden, int group, int64_t chunk_tokens,
-                           const float *q_norm_w, const float *k_norm_w, float eps, const float *rope_cs,
-                           int rot_dim, void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream) {
+int streamed_qkv_proj_ex(const void *x, const void *w_qkv, int64_t n, int hidden, int group, int64_t chunk_tokens,
+                         const float *q_norm_w, const float *k_norm_w, float eps, const float *rope_cs, int rot_dim,
+                         int sections, void *q_out, const kvq_range *ranges, int n_ranges, kvq_stream_t stream) {
+    if (sections < 1 || sections > 3) return KVQ_ERR_ARG;
+    const bool want_q = sections & KVQ_SECTION_Q, want_kv = sections & KVQ_SECTION_KV;
     if (rope_cs && rot_dim != 64 && rot_dim != 128) return KVQ_ERR_UNSUPPORTED;
     if (rope_cs && !aligned16(rope_cs)) return KVQ_ERR_ALIGN;
-    if (!x || !w_qkv || !q_out) return KVQ_ERR_ARG;
+    if (!x || !w_qkv || (want_q && !q_out)) return KVQ_ERR_ARG;
     if (n < 1 || n > (int64_t(1) << 31) - 256 || !valid_hidden(hidden) || !valid_group(group) || chunk_tokens < 0)
         return KVQ_ERR_ARG;
     if (!(eps >= 0.0f)) return KVQ_ERR_ARG;
-    if (x == q_out) return KVQ_ERR_ARG;
-    if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q_out)) return KVQ_ERR_ALIGN;
+    if (want_q && x == q_out) return KVQ_ERR_ARG;
+    if (!aligned16(x) || !aligned16(w_qkv) || (want_q && !aligned16(q_out))) return KVQ_ERR_ALIGN;
     if ((q_norm_w && (reinterpret_cast<uintptr_t>(q_norm_w) & 3u)) ||
         (k_norm_w && (reinterpret_cast<uintptr_t>(k_norm_w) & 3u)))
         return KVQ_ERR_ALIGN;
     RangeTable t;
-    int st = check_range_table(ranges, n_ranges, n, hidden, group, true, &t);
-    if (st) return st;
-    return launch_qkv_proj(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps, q_out, t,
-                           reinterpret_cast<cudaStream_t>(stream), rope_cs, rot_dim);
+    std::memset(&t, 0, sizeof(t));
+    if (want_kv) {
+        const int st = check_range_table(ranges, n_ranges, n, hidden, group, true, &t);
+        if (st) return st;
+    }
+    return launch_qkv_proj(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps,
+                           want_q ? q_out : nullptr, t, reinterpret_cast<cudaStream_t>(stream), rope_cs, rot_dim,
+                           sections);
 }
 
 int streamed_qkv_proj(const void *x, const void *w_qkv, int64_t n, int hidden, int group, int64_t chunk_tokens,
@@ -239,8 +245,21 @@ int streamed_qkv_proj(const void *x, const void *w_qkv, int64_t n, int hidden, i
     r.v_codes = v_codes;
     r.k_scales = k_scales;
     r.v_scales = v_scales;
-    return streamed_qkv_proj_mixed(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps, q_out, &r, 1,
-                                   stream);
+    int st = streamed_qkv_proj_mixed(x, w_qkv, n, hidden, group, chunk_tokens, q_norm_w, k_norm_w, eps, q_out, &r, 1,
+                                     stream);
+    if (st || r.cap == n) return st;
+    // the whole store is the caller's: its pad rows n .. cap-1 of every head become zero
+    const size_t heads = static_cast<size_t>(hidden / 128), pad = static_cast<size_t>(r.cap - n);
+    const size_t cb = 64, sb = 2 * static_cast<size_t>(128 / group);  // bytes per row: codes, scales
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    for (void *base : {k_codes, v_codes})
+        if (e == cudaSuccess)
+            e = cudaMemset2DAsync(static_cast<uint8_t *>(base) + n * cb, r.cap * cb, 0, pad * cb, heads, s);
+    for (void *base : {k_scales, v_scales})
+        if (e == cudaSuccess)
+            e = cudaMemset2DAsync(static_cast<uint8_t *>(base) + n * sb, r.cap * sb, 0, pad * sb, heads, s);
+    return cuda_status(e);
 }
 
 

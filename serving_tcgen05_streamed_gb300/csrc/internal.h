@@ -32,8 +32,7 @@ cudaError_t launch_kv_unpack(const void *k_codes, const void *v_codes, const voi
 // Returns 0 on success, a kvq_status otherwise.
 int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int group, int64_t chunk_tokens,
                     const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, const RangeTable &ranges,
-                    cudaStream_t s, const float *rope_cs = nullptr,
-                    int rot_dim = 0);
+                    cudaStream_t s, const float *rope_cs = nullptr, int rot_dim = 0, int sections = 3);
 int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int hidden, int group, float sm_scale,
                      int out_fp32, void *out, cudaStream_t s, int causal = 0, int64_t q_pos0 = 0);
 cudaError_t launch_selftest_wait(uint64_t ns, cudaStream_t s);

@@ -50,6 +50,8 @@ struct ProjParams {
     int64_t n;
     int hidden;
     int m_tiles, n_tiles, k_blocks;
+    int col_tile0;  // first 256-column tile of W walked (tiles col_tile0 .. col_tile0 + n_tiles - 1)
+    int sections;   // bit 0: write Q, bit 1: write K and V (128-column halves of other sections are skipped)
     int chunk_m_tiles;
     int64_t total_tiles;
     const float *q_norm_w;
@@ -66,7 +68,7 @@ __device__ __forceinline__ void tile_coords(int64_t T, const ProjParams &p, int 
     const int64_t local = T - c * per_chunk;
     const int m0 = static_cast<int>(c) * p.chunk_m_tiles;
     const int mc = min(p.chunk_m_tiles, p.m_tiles - m0);
-    n_idx = static_cast<int>(local / mc);
+    n_idx = p.col_tile0 + static_cast<int>(local / mc);
     m_idx = m0 + static_cast<int>(local % mc);
 }
 
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(raw[i]);
                 const int sect = gcol / C;
+                if (!((p.sections >> (sect == 0 ? 0 : 1)) & 1)) continue;
                 const int head = (gcol - sect * C) >> 7;
                 if (sect == 0) {
                     if (p.q_norm_w) rmsnorm128(v, p.q_norm_w, p.eps);
@@ -297,13 +300,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (sect == 1 && row < p.n) rope_split_half<ROT>(v, p.rope_cs + row * ROT);
                     }
                     rotate128_thread(v);
-                    // the range holding this token (rows past n belong to the last range's padding)
+                    // the range holding this token; rows past a range's len are never
+                    // written (a range may be a window into a larger store)
                     int g = 0;
                     for (int i = 1; i < p.ranges.n; ++i)
                         if (row >= p.ranges.r[i].start) g = i;
                     const RangeDev &R = p.ranges.r[g];
                     const int64_t rr = row - R.start;
-                    if (rr < R.cap && (row < p.n || g == p.ranges.n - 1)) {
+                    if (row < p.n && rr < R.len) {
                         const bool is_k = (sect == 1);
                         if (R.bits == 4) {
                             uint8_t *cr = (is_k ? R.k_codes : R.v_codes) + (head * R.cap + rr) * 64;
@@ -352,7 +356,7 @@ cudaError_t launch_rot(const CUtensorMap &tm_x, const CUtensorMap &tm_w, const P
 
 int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int group, int64_t chunk_tokens,
                     const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, const RangeTable &ranges,
-                    cudaStream_t s, const float *rope_cs, int rot_dim) {
+                    cudaStream_t s, const float *rope_cs, int rot_dim, int sections) {
     alignas(64) CUtensorMap tm_x, tm_w;
     if (encode_tmap_2d(&tm_x, x, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(n),
                        static_cast<uint64_t>(hidden) * 2, BK, BM))
@@ -364,7 +368,11 @@ int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int gro
     p.n = n;
     p.hidden = hidden;
     p.m_tiles = static_cast<int>((n + BM - 1) / BM);
-    p.n_tiles = (3 * hidden + BN - 1) / BN;
+    // the W rows (output columns) of the requested sections: Q = [0, C), K and V = [C, 3C)
+    const int c0 = (sections & 1) ? 0 : hidden, c1 = (sections & 2) ? 3 * hidden : hidden;
+    p.col_tile0 = c0 / BN;
+    p.n_tiles = (c1 + BN - 1) / BN - p.col_tile0;
+    p.sections = sections;
     p.k_blocks = hidden / BK;
     int64_t cm = chunk_tokens <= 0 ? p.m_tiles : (chunk_tokens + BM - 1) / BM;
     if (cm > p.m_tiles) cm = p.m_tiles;

@@ -98,12 +98,21 @@ def test_argument_errors_are_reported_before_any_launch():
     assert lib.packed_kv_attention(a16, 10, a16, odd, a16, a16, 5, 1024, 32, 0.0, 0, a16, S) == kvq.KVQ_ERR_ALIGN
     # RoPE: rot_dim 64 or 128 only, 16-byte aligned table
     R1 = (_lib._Range * 1)(_lib._Range(0, 10, 128, 4, 0, a16.value, a16.value, a16.value, a16.value))
-    assert lib.streamed_qkv_proj_rope(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, a16, 32, P(2 << 20), R1, 1, S) \
+    assert lib.streamed_qkv_proj_ex(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, a16, 32, 3, P(2 << 20), R1, 1, S) \
         == kvq.KVQ_ERR_UNSUPPORTED
-    assert lib.streamed_qkv_proj_rope(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, odd, 128, P(2 << 20), R1, 1, S) \
+    assert lib.streamed_qkv_proj_ex(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, odd, 128, 3, P(2 << 20), R1, 1, S) \
         == kvq.KVQ_ERR_ALIGN
-    assert lib.streamed_qkv_proj_rope(None, a16, 10, 1024, 32, 0, None, None, 1e-6, a16, 128, P(2 << 20), R1, 1, S) \
+    assert lib.streamed_qkv_proj_ex(None, a16, 10, 1024, 32, 0, None, None, 1e-6, a16, 128, 3, P(2 << 20), R1, 1, S) \
         == kvq.KVQ_ERR_ARG
+    # sections: 1..3 only; Q-only needs no ranges, K/V-only no q_out
+    assert lib.streamed_qkv_proj_ex(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, None, 0, 0, P(2 << 20), R1, 1, S) \
+        == kvq.KVQ_ERR_ARG
+    assert lib.streamed_qkv_proj_ex(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, None, 0, 4, P(2 << 20), R1, 1, S) \
+        == kvq.KVQ_ERR_ARG
+    assert lib.streamed_qkv_proj_ex(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, None, 0, 1, None, R1, 1, S) \
+        == kvq.KVQ_ERR_ARG  # Q asked for, no q_out
+    assert lib.streamed_qkv_proj_ex(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, None, 0, 2, None, None, 0, S) \
+        == kvq.KVQ_ERR_ARG  # K/V asked for, no ranges
     # causal: a negative query position, and the checks it shares
     assert lib.packed_kv_attention_causal(a16, 10, -1, a16, a16, a16, a16, 5, 1024, 32, 0.0, 0, a16, S) \
         == kvq.KVQ_ERR_ARG

@@ -26,7 +26,7 @@ def _table(n, rot_dim, base=10000.0, offset=0):
 def _run(x, w, cs, qn=None, kn=None, chunk=0):
     n, C = x.shape
     store = kvq.PackedKV.empty(n, C, 32, 4, "cuda")
-    q = kvq.streamed_qkv_proj_rope(x.cuda(), w.cuda(), [store], torch.from_numpy(cs).cuda(), chunk_tokens=chunk,
+    q = kvq.streamed_qkv_proj_ex(x.cuda(), w.cuda(), [store], torch.from_numpy(cs).cuda(), chunk_tokens=chunk,
                                    q_norm_w=None if qn is None else qn.cuda(),
                                    k_norm_w=None if kn is None else kn.cuda())
     torch.cuda.synchronize()
