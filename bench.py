@@ -260,7 +260,8 @@ def run_gpu(args, wl, world, rank, local):
     if world > 1:  # independent problems per rank
         x = x.roll(rank * 7, dims=0)
     causal = args.workload == "causal"
-    wl_label = wl.name + (", causal attention" if causal else "") + (", RoPE 128 in the projection" if args.rope else "")
+    wl_label = (wl.name + (", causal attention" if causal else "") + (", RoPE 128 in the projection" if args.rope else "")
+                + (", text and audio query rows routed to an INT8 store of every key" if args.route_av else ""))
     rope = None
     if args.rope:  # split-half RoPE table of Q and K: token position t, frequencies 10000^(-2i/128)
         pos = torch.arange(n, dtype=torch.float64, device=dev)[:, None]
@@ -277,6 +278,35 @@ def run_gpu(args, wl, world, rank, local):
         stores = [kvq.PackedKV.empty(n, C, 32, 4, dev)]
     store = stores[0]
     q = torch.empty((n, C), dtype=torch.bfloat16, device=dev)
+    route = bool(args.route_av) and mixed
+    fine = kvq.PackedKV.empty(n, C, 32, 8, dev) if route else None  # INT8 K/V of every key for the routed rows
+    # query rows routed to the fine store: the text and audio segments
+    routed_segs, start_ = [], 0
+    for name_, seg_n, _ in (inputs.MIXED_SEGMENTS if mixed else ()):
+        routed_segs.append((start_, seg_n, route and name_ in ("text", "audio")))
+        start_ += seg_n
+
+    def attend_rows(qc, s0):
+        """Attention of query rows s0 .. s0+len(qc)-1, output over qc."""
+        if mixed and not route:
+            kvq.packed_kv_attention_mixed(qc, stores, out=qc, stream=stream)
+        elif mixed:
+            for a, ln_, to_fine in routed_segs:
+                lo, hi = max(a, s0), min(a + ln_, s0 + qc.shape[0])
+                if lo >= hi:
+                    continue
+                part = qc[lo - s0:hi - s0]
+                kvq.packed_kv_attention_mixed(part, [fine] if to_fine else stores, out=part, stream=stream)
+        elif causal:
+            kvq.packed_kv_attention_causal(qc, store, q_pos0=s0, out=qc, stream=stream)
+        else:
+            kvq.packed_kv_attention(qc, store, out=qc, stream=stream)
+
+    def project_fine(xc, s0, ln):
+        if route:
+            kvq.streamed_qkv_proj_ex(xc, w, [fine.rows(s0, ln)], rope[s0:s0 + ln] if rope is not None else None,
+                                     sections=kvq.SECTION_KV, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
+                                     k_norm_w=kn, stream=stream)
 
     def project(xin):
         if rope is not None:
@@ -288,14 +318,10 @@ def run_gpu(args, wl, world, rank, local):
         else:
             kvq.streamed_qkv_proj(xin, w, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, q_out=q,
                                   store=store, stream=stream)
+        project_fine(xin, 0, n)
 
     def attend():
-        if mixed:
-            kvq.packed_kv_attention_mixed(q, stores, out=q, stream=stream)
-        elif causal:
-            kvq.packed_kv_attention_causal(q, store, out=q, stream=stream)
-        else:
-            kvq.packed_kv_attention(q, store, out=q, stream=stream)
+        attend_rows(q, 0)
 
     def step():
         project(x)
@@ -371,14 +397,10 @@ def run_gpu(args, wl, world, rank, local):
                 kvq.streamed_qkv_proj_mixed(x_dev[s0:s0 + ln], w, windows(s0, ln), group=32,
                                             chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn,
                                             q_out=q[s0:s0 + ln], stream=stream)
+            project_fine(x_dev[s0:s0 + ln], s0, ln)
         for s0, ln in out_chunks:
             qc = q[s0:s0 + ln]
-            if mixed:
-                kvq.packed_kv_attention_mixed(qc, stores, out=qc, stream=stream)
-            elif causal:
-                kvq.packed_kv_attention_causal(qc, store, q_pos0=s0, out=qc, stream=stream)
-            else:
-                kvq.packed_kv_attention(qc, store, out=qc, stream=stream)
+            attend_rows(qc, s0)
             ev = torch.cuda.Event()
             ev.record(stream)
             copy.wait_event(ev)
@@ -423,6 +445,7 @@ def run_gpu(args, wl, world, rank, local):
             kvq.streamed_qkv_proj_ex(xb[b][:ln], w, windows(s0, ln), rope[s0:s0 + ln] if rope is not None else None,
                                      sections=kvq.SECTION_KV, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
                                      k_norm_w=kn, stream=stream)
+            project_fine(xb[b][:ln], s0, ln)
             ev["p1"][b].record(stream)
         for i, (s0, ln) in enumerate(out_chunks):
             b = i % 2
@@ -436,12 +459,7 @@ def run_gpu(args, wl, world, rank, local):
                                           sections=kvq.SECTION_Q, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn,
                                           k_norm_w=kn, q_out=qb[b][:ln], stream=stream)
             ev["qp"][b].record(stream)
-            if mixed:
-                kvq.packed_kv_attention_mixed(qc, stores, out=qc, stream=stream)
-            elif causal:
-                kvq.packed_kv_attention_causal(qc, store, q_pos0=s0, out=qc, stream=stream)
-            else:
-                kvq.packed_kv_attention(qc, store, out=qc, stream=stream)
+            attend_rows(qc, s0)
             ev["attn"][b].record(stream)
             if i + 1 < len(out_chunks):  # next chunk's x, once the projection of chunk i-1 has read xq[1-b]
                 s1, l1 = out_chunks[i + 1]
@@ -464,7 +482,7 @@ def run_gpu(args, wl, world, rank, local):
     e2e2_s = max_over_ranks(world, (time.perf_counter() - t0) / e2e_steps)
     peak2_gib = (torch.cuda.max_memory_allocated(dev) - mem0) / GiB
     # device memory the step holds beyond what stays resident across steps (W, norms, table)
-    resident_gib = (sum(st_.nbytes() for st_ in stores)) / GiB
+    resident_gib = (sum(st_.nbytes() for st_ in stores) + (fine.nbytes() if route else 0)) / GiB
     assert kvq.device_status() == kvq.KVQ_OK
 
     # ------------------------------------------------------------ roofline of the dominant kernel (attention)
@@ -500,6 +518,7 @@ def run_gpu(args, wl, world, rank, local):
             "data": "synthetic (seeded generators; random-init weights of the H3 block shape)",
             "config": {"workload": wl_label, "n_tokens": n, "hidden": C,
                        "heads": wl.heads, "group": 32, "causal": causal, "rope": rope is not None,
+                       "route_av": route,
                        "kv_bits": "8/4 by token range" if mixed else 4, "chunk_tokens": wl.chunk_tokens,
                        "qk_rmsnorm": True,
                        "l2": f"inputs larger than L2 (x {n * C * 2 / GiB:.2f} GiB, packed K/V "
@@ -605,6 +624,8 @@ def main():
                     help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling); "
                          "mixed: N=217,088 with INT8 conditioning ranges; causal: the N=152,263 block with causal "
                          "attention; sweep: pack/unpack bandwidth")
+    ap.add_argument("--route-av", action="store_true",
+                    help="mixed workload: text and audio query rows attend an INT8 store of every key")
     ap.add_argument("--rope", action="store_true",
                     help="split-half RoPE (rot_dim 128) of Q and K in the projection epilogue")
     ap.add_argument("--sweep-n", type=int, nargs="+", default=None,
