@@ -79,7 +79,7 @@ constexpr int BQT = 128;       // query rows per tile
 constexpr int NQT = 2;         // query tiles per CTA
 constexpr int BQ = BQT * NQT;  // query rows per CTA
 constexpr int BKV = 128;       // keys per tile
-constexpr int KV_STAGES = 2;   // K^ / V^ shared-memory stages
+constexpr int KV_STAGES = 3;   // K^ / V^ shared-memory stages
 constexpr int NUM_DQ_THREADS = 192;  // warps 8-11 and 14-15
 constexpr int NUM_DQ_WARPS = NUM_DQ_THREADS / 32;
 constexpr int NUM_SM_WARPS = 4;  // per query tile
@@ -135,6 +135,8 @@ struct SmemLayout {
     static constexpr int BAR = STG + Staging::BYTES;
     static constexpr int BYTES = BAR + 256;
 };
+static_assert((15 + 3 * KV_STAGES) * 8 + 8 <= 256, "barriers and the TMEM slot overflow their area");
+static_assert(SmemLayout::BYTES <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
@@ -428,6 +430,14 @@ __device__ __forceinline__ int cta_tiles(const AttnParams &p) {
     return need < p.total_tiles ? static_cast<int>(need) : p.total_tiles;
 }
 
+// A shared-memory matrix descriptor moved by `bytes`: the start address is
+// the low 14-bit field (address / 16), and shared-memory addresses stay below
+// 2^18 bytes, so the sum never carries out of it.  Descriptors are built once
+// and moved with one 32-bit add per MMA.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+    return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + (bytes >> 4));
+}
+
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
     tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
     tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
@@ -453,18 +463,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint8_t *sStg = smem + L::STG;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR);
     uint64_t *q_tma = bars + 0;
-    uint64_t *q_ready = bars + 1;   // even CTA: Q of both CTAs converted
-    uint64_t *kv_full = bars + 2;   // [KV_STAGES], even CTA: both CTAs' halves decoded
-    uint64_t *k_empty = bars + 4;   // [KV_STAGES]: K^ stage read by its last Q.K^T
-    uint64_t *s_full = bars + 6;    // [NQT]
-    uint64_t *p_full = bars + 8;    // [NQT], even CTA: P of both CTAs in TMEM
-    uint64_t *pv_done = bars + 10;  // [NQT]
-    uint64_t *stg_full = bars + 12;   // [SL::STAGES]
-    uint64_t *stg_empty = bars + 14;  // [SL::STAGES]
-    uint64_t *v_empty = bars + 16;    // [KV_STAGES]: V^ stage read by its last P.V^
-    uint64_t *drain = bars + 18;      // even CTA: every MMA has completed
-    uint64_t *p_half = bars + 19;     // [NQT], even CTA: P of keys 0-63 of both CTAs in TMEM
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 21);
+    uint64_t *q_ready = bars + 1;             // even CTA: Q of both CTAs converted
+    uint64_t *s_full = bars + 2;              // [NQT]
+    uint64_t *p_full = bars + 4;              // [NQT], even CTA: P of both CTAs in TMEM
+    uint64_t *p_half = bars + 6;              // [NQT], even CTA: P of keys 0-63 of both CTAs in TMEM
+    uint64_t *pv_done = bars + 8;             // [NQT]
+    uint64_t *stg_full = bars + 10;           // [SL::STAGES]
+    uint64_t *stg_empty = bars + 12;          // [SL::STAGES]
+    uint64_t *drain = bars + 14;              // even CTA: every MMA has completed
+    uint64_t *kv_full = bars + 15;            // [KV_STAGES], even CTA: both CTAs' halves decoded
+    uint64_t *k_empty = kv_full + KV_STAGES;  // [KV_STAGES]: K^ stage read by its last Q.K^T
+    uint64_t *v_empty = k_empty + KV_STAGES;  // [KV_STAGES]: V^ stage read by its last P.V^
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(v_empty + KV_STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -524,15 +534,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t qa = smem_u32(sQ);
                     bool ok = mbar_wait_cluster(q_ready, 0, abort_flag, &g_err_attn);
                     tc_fence_after();
+                    const uint64_t dq = make_sdesc_sw128(qa);
+                    const uint64_t dk = make_sdesc_sw128(smem_u32(sK));
+                    const uint64_t dv = make_sdesc_sw128_mn(smem_u32(sV), V_TILE_BYTES);
                     auto issue_s = [&](int j, int t) {  // S_t(j) = Q_t . K^_j^T over the pair
-                        const uint32_t kb = smem_u32(sK + (j % KV_STAGES) * K_TILE_BYTES);
+                        const uint64_t kd = desc_add(dk, (j % KV_STAGES) * K_TILE_BYTES);
                         const uint32_t d = tmem + tm_s(t);
-                        const uint32_t q = qa + t * Q_TILE_BYTES;
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
-                            const uint32_t kin = (k & 3) * 32;
-                            mma_f16_ss_pair(d, make_sdesc_sw128(q + (k >> 2) * Q_HALF_BYTES + kin),
-                                            make_sdesc_sw128(kb + (k >> 2) * K_HALF_BYTES + kin), idesc, k > 0);
+                            const uint32_t kin = (k >> 2) * Q_HALF_BYTES + (k & 3) * 32;
+                            mma_f16_ss_pair(d, desc_add(dq, t * Q_TILE_BYTES + kin),
+                                            desc_add(kd, (k >> 2) * K_HALF_BYTES + (k & 3) * 32), idesc, k > 0);
                         }
                         mma_commit_pair(&s_full[t], kPairMask);
                     };
@@ -547,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     }
                     for (int j = 0; ok && j < T; ++j) {
                         const int st = j % KV_STAGES;
-                        const uint32_t vb = smem_u32(sV + st * V_TILE_BYTES);
+                        const uint64_t vd = desc_add(dv, st * V_TILE_BYTES);
                         for (int t = 0; t < NQT && ok; ++t) {
                             // O_t += P_t(j) . V^_j, P_t read from TMEM (the first 64 columns of S_t);
                             // keys 0-63 go as soon as their P is written, keys 64-127 after
@@ -560,7 +572,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                                 for (int k = 4 * hf; k < 4 * hf + 4; ++k) {  // keys 16k .. 16k+15: 16 rows of V^
                                     mma_f16_ts_pair(tmem + tm_o(t), tmem + tm_s(t) + k * 8,
-                                                    make_sdesc_sw128_mn(vb + k * 2048, V_TILE_BYTES), idesc_pv,
+                                                    desc_add(vd, k * 2048), idesc_pv,
                                                     (j > 0 || k > 0) ? 1u : 0u);
                                 }
                             }
