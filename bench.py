@@ -504,7 +504,7 @@ def run_gpu(args, wl, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not mixed and not causal and rope is None:
-        del x_host, out_host, x_dev
+        del x_host, out_host
         sample = CpuOracleSample(wl, seed=7, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
         t_block = sample.run()
         cpu = {"value": (fp + fa) / t_block / 1e12, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
