@@ -112,14 +112,14 @@ struct AttnParams {
     int64_t q_pos0;  // single store only
 };
 
-// Staging buffers of packed codes, filled by bulk copies: two 16 KB stages.
+// Staging buffers of packed codes, filled by bulk copies: three 16 KB stages.
 // An INT4 tile takes one stage: the CTA's 64 K rows (4 KB) at offset 0 and
 // all 128 V rows (8 KB, of which the CTA decodes its half of each row) at
-// offset 4096.  An INT8 tile takes two consecutive stages: 64 K rows (8 KB)
-// in the first, 128 V rows (16 KB) in the second.  The loader and the
-// dequantisers walk the same running stage counter.
+// offset 4096.  An INT8 tile takes two consecutive stages (in ring order):
+// 64 K rows (8 KB) in the first, 128 V rows (16 KB) in the second.  The
+// loader and the dequantisers walk the same running stage counter.
 struct Staging {
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = 3;
     static constexpr int STAGE_BYTES = 16384;
     static constexpr int BYTES = STAGES * STAGE_BYTES;
     static constexpr int INT4_V_OFFSET = 4096;
@@ -135,7 +135,8 @@ struct SmemLayout {
     static constexpr int BAR = STG + Staging::BYTES;
     static constexpr int BYTES = BAR + 256;
 };
-static_assert((15 + 3 * KV_STAGES) * 8 + 8 <= 256, "barriers and the TMEM slot overflow their area");
+static_assert((11 + 2 * Staging::STAGES + 3 * KV_STAGES) * 8 + 8 <= 256,
+              "barriers and the TMEM slot overflow their area");
 static_assert(SmemLayout::BYTES <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -468,10 +469,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint64_t *p_full = bars + 4;              // [NQT], even CTA: P of both CTAs in TMEM
     uint64_t *p_half = bars + 6;              // [NQT], even CTA: P of keys 0-63 of both CTAs in TMEM
     uint64_t *pv_done = bars + 8;             // [NQT]
-    uint64_t *stg_full = bars + 10;           // [SL::STAGES]
-    uint64_t *stg_empty = bars + 12;          // [SL::STAGES]
-    uint64_t *drain = bars + 14;              // even CTA: every MMA has completed
-    uint64_t *kv_full = bars + 15;            // [KV_STAGES], even CTA: both CTAs' halves decoded
+    uint64_t *stg_full = bars + 10;              // [SL::STAGES]
+    uint64_t *stg_empty = stg_full + SL::STAGES;  // [SL::STAGES]
+    uint64_t *drain = stg_empty + SL::STAGES;    // even CTA: every MMA has completed
+    uint64_t *kv_full = drain + 1;               // [KV_STAGES], even CTA: both CTAs' halves decoded
     uint64_t *k_empty = kv_full + KV_STAGES;  // [KV_STAGES]: K^ stage read by its last Q.K^T
     uint64_t *v_empty = k_empty + KV_STAGES;  // [KV_STAGES]: V^ stage read by its last P.V^
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(v_empty + KV_STAGES);
