@@ -11,9 +11,11 @@
 // one 128-wide head vector, 32 consecutive elements each, so five of the seven
 // butterfly stages and (for groups of 32) the whole group absmax stay inside
 // a lane, and a lane's codes leave in one 16-byte store.  A warp works on 8
-// tokens of one head slot at a time (K heads, then V heads), two such passes
-// loaded ahead of the arithmetic; a block of 8 warps covers 8 head slots x 32
-// tokens.
+// tokens of one head slot at a time (K heads, then V heads); a block of 8
+// warps covers 8 head slots x 32 tokens.  The pack kernel is held to 64
+// registers, so four blocks (32 warps) share an SM and hide the load latency:
+// one pass of 8 tokens at a time fits without spills, and this measured
+// 1.5-4 % faster than two passes loaded ahead at 80 registers, 3 blocks / SM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -31,7 +33,7 @@ constexpr int kTokensPerBlock = 32;
 constexpr int kPass = 8;  // tokens per warp pass (4 lanes per token)
 
 template <int GROUP, int BITS>
-__global__ void __launch_bounds__(kWarps * 32) rotate_quant_pack_kernel(const __nv_bfloat16 *__restrict__ kv,
+__global__ void __launch_bounds__(kWarps * 32, 4) rotate_quant_pack_kernel(const __nv_bfloat16 *__restrict__ kv,
                                                                          int64_t n, int64_t cap, int heads,
                                                                          int64_t ld, uint8_t *__restrict__ k_codes,
                                                                          uint8_t *__restrict__ v_codes,
@@ -51,37 +53,31 @@ __global__ void __launch_bounds__(kWarps * 32) rotate_quant_pack_kernel(const __
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock + (lane >> 2);
 
 #pragma unroll 1
-    for (int p = 0; p < kTokensPerBlock / kPass; p += 2) {
-        uint4 raw[2][4];
+    for (int p = 0; p < kTokensPerBlock / kPass; ++p) {
+        const int64_t t = t0 + p * kPass;
+        uint4 raw[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t t = t0 + (p + u) * kPass;
+        for (int i = 0; i < 4; ++i)
+            raw[i] = (t < n) ? ld_global_nc_v4(src + t * ld + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
+        float v[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                raw[u][i] = (t < n) ? ld_global_nc_v4(src + t * ld + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
-        }
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t t = t0 + (p + u) * kPass;
-            float v[32];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t w[4] = {raw[u][i].x, raw[u][i].y, raw[u][i].z, raw[u][i].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
-                    v[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
-                }
+            for (int e = 0; e < 4; ++e) {
+                v[8 * i + 2 * e] = __uint_as_float(w[e] << 16);
+                v[8 * i + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
             }
-            rotate128_quad(v, lane);
-            uint32_t words[BITS];
-            uint16_t sbits;
-            quant128_quad<GROUP, BITS>(v, words, sbits);
-            uint4 *dst = reinterpret_cast<uint4 *>(codes + t * CB + q * (CB / 4));
-#pragma unroll
-            for (int i = 0; i < BITS / 4; ++i) st_global_v4(dst + i, make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]));
-            if ((q % (GROUP / 32)) == 0) scales[t * SG + q / (GROUP / 32)] = sbits;
         }
+        rotate128_quad(v, lane);
+        uint32_t words[BITS];
+        uint16_t sbits;
+        quant128_quad<GROUP, BITS>(v, words, sbits);
+        uint4 *dst = reinterpret_cast<uint4 *>(codes + t * CB + q * (CB / 4));
+#pragma unroll
+        for (int i = 0; i < BITS / 4; ++i)
+            st_global_v4(dst + i, make_uint4(words[4 * i], words[4 * i + 1], words[4 * i + 2], words[4 * i + 3]));
+        if ((q % (GROUP / 32)) == 0) scales[t * SG + q / (GROUP / 32)] = sbits;
     }
 }
 
