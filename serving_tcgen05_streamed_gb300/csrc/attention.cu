@@ -44,7 +44,10 @@
 //   warp 12    TMA of the CTA's Q tiles, TMEM allocation (jointly with the
 //              peer CTA) and, in the even CTA, the single MMA thread.
 //   warp 13    bulk copies (TMA engine) of each tile's codes into the staging
-//              buffer, one tile ahead.
+//              ring, as far ahead as its three stages allow (three INT4
+//              tiles, or one INT8 tile and part of the next).
+// K^ and V^ have three shared-memory stages each, so the dequantisers can
+// work up to two tiles ahead of the tensor core.
 // The MMA thread waits on barriers of the even CTA that the threads of both
 // CTAs arrive on; its commits arrive on the same barriers of both CTAs.
 // Registers are redistributed with setmaxnreg: 168 per softmax thread, 88
