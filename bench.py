@@ -46,18 +46,22 @@ def flops(n: int, C: int, causal: bool = False) -> tuple[float, float]:
 ATTENTION_SOURCES = ("attention.cu", "ptx.cuh", "quant.cuh", "internal.h")
 
 
+def code_text(text):
+    """C/CUDA source without comments, whitespace runs collapsed to one space."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def attention_code_sha256():
     """sha256 of the attention kernel's sources with comments and whitespace runs
     removed: the key under which DRAM counters of an ncu capture stay valid."""
     import hashlib
-    import re
     h = hashlib.sha256()
     for name in ATTENTION_SOURCES:
         with open(os.path.join(ROOT, "serving_tcgen05_streamed_gb300", "csrc", name)) as f:
-            text = f.read()
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        h.update((name + "\0" + " ".join(text.split()) + "\0").encode())
+            h.update((name + "\0" + code_text(f.read()) + "\0").encode())
     return h.hexdigest()
 
 

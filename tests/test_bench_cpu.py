@@ -1,0 +1,32 @@
+"""Host logic of bench.py that needs no GPU: the key of the DRAM-traffic record."""
+import importlib.util
+import json
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_code_text_ignores_comments_and_layout_but_not_code():
+    b = _bench()
+    a = "int x = 1;  // one\n/* block\n comment */ float y = x * 2.0f;\n"
+    assert b.code_text(a) == b.code_text("int x = 1;\nfloat   y = x * 2.0f;")
+    assert b.code_text(a) != b.code_text("int x = 2; float y = x * 2.0f;")
+
+
+def test_attention_code_hash_is_stable_and_the_record_is_well_formed():
+    b = _bench()
+    h = b.attention_code_sha256()
+    assert re.fullmatch(r"[0-9a-f]{64}", h) and h == b.attention_code_sha256()
+    with open(os.path.join(ROOT, "profiles", "attention_traffic.json")) as f:
+        rec = json.load(f)
+    assert re.fullmatch(r"[0-9a-f]{64}", rec["code_sha256"])
+    assert rec["bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    assert rec["workload"].startswith("H3 Ref2VA block N=152263")
