@@ -8,7 +8,7 @@ import torch
 import oracle
 import serving_tcgen05_streamed_gb300 as kvq
 from serving_tcgen05_streamed_gb300 import inputs
-from tests._util import bits16, codes_as_int, to_token_major
+from tests._util import bf16_ulp, bits16, codes_as_int, to_token_major
 
 pytestmark = pytest.mark.gpu
 
@@ -69,5 +69,58 @@ def test_mixed_attention_matches_oracle(lens):
         start += st.n
     ref = oracle.attention_mixed(bits16(q), ranges)
     got = out.cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref).max() <= 1e-2
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-3
+
+
+@pytest.mark.slow
+def test_mixed_block_full_size_sampled_rows():
+    # The mixed-precision block at full size (N = 217,088: text, reference and audio
+    # at INT8, generated video at INT4), projected and attended as the benchmark runs
+    # it.  The oracle checks sampled token rows of the projection in every segment and
+    # sampled query rows of the attention, each exact per row.
+    wl = inputs.MIXED
+    x, w, qn, kn = inputs.block_inputs(wl, device="cuda")
+    n, C = x.shape
+    segs = inputs.MIXED_SEGMENTS
+    assert sum(sn for _, sn, _ in segs) == n
+    stores = [kvq.PackedKV.empty(sn, C, 32, bits, "cuda") for _, sn, bits in segs]
+    q = kvq.streamed_qkv_proj_mixed(x, w, stores, group=32, chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn)
+    out = kvq.packed_kv_attention_mixed(q, stores, out_fp32=True)
+    torch.cuda.synchronize()
+    assert kvq.device_status() == kvq.KVQ_OK
+    rng = np.random.default_rng(17)
+    wb, qn_np, kn_np = bits16(w), qn.cpu().numpy(), kn.cpu().numpy()
+    picks, start = [], 0
+    for (name, sn, bits), st in zip(segs, stores):
+        local = np.unique(np.concatenate([[0, sn - 1], rng.integers(0, sn, 2)]))
+        rows = start + local
+        picks.append(rows)
+        ref = oracle.qkv_proj(bits16(x[torch.as_tensor(rows, device="cuda")]), wb, bits=bits, q_norm_w=qn_np,
+                              k_norm_w=kn_np, eps=1e-6)
+        got_q = bits16(q[torch.as_tensor(rows, device="cuda")]).view(np.uint16)
+        qf = (got_q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        rf = ref["q_f32"].astype(np.float64)
+        rms = np.sqrt(np.mean(rf.reshape(rf.shape[0], -1, 128) ** 2, axis=-1, keepdims=True))
+        floor = np.broadcast_to(1e-4 * rms, rms.shape[:2] + (128,)).reshape(rf.shape)
+        assert np.all(np.abs(qf - rf) <= bf16_ulp(rf) * 1.0001 + floor), name
+        for cname, sname in (("k_codes", "k_scales"), ("v_codes", "v_scales")):
+            gc = to_token_major(getattr(st, cname), local)
+            gs = to_token_major(getattr(st, sname), local).view(np.uint16)
+            d = np.abs(codes_as_int(gc, bits).astype(np.int32) - codes_as_int(ref[cname], bits))
+            assert d.max() <= 1 and np.mean(d != 0) <= 1e-3, (name, cname)
+            ds = np.abs(gs.astype(np.int32) - ref[sname].astype(np.int32))
+            assert ds.max() <= 1 and np.mean(ds != 0) <= 2e-2, (name, sname)
+        start += sn
+    # attention: the sampled query rows against every key of the four stores
+    rows = np.concatenate(picks)
+    ranges, start = [], 0
+    for st in stores:
+        d = _np_store(st)
+        ranges.append(dict(start=start, **{k: d[k] for k in ("k_codes", "v_codes", "k_scales", "v_scales", "bits",
+                                                               "len")}))
+        start += st.n
+    ref = oracle.attention_mixed(bits16(q[torch.as_tensor(rows, device="cuda")]), ranges)
+    got = out[torch.as_tensor(rows, device="cuda")].cpu().numpy().astype(np.float64)
     assert np.abs(got - ref).max() <= 1e-2
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 5e-3
