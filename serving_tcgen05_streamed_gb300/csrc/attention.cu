@@ -68,6 +68,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdlib>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -689,35 +690,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         };
         if (ok && T > 0) prefetch_scales();
         int k = 0;  // running stage counter, as the loader's
-        for (int j = 0; ok && j < T && !*abort_flag; ++j, cur.next(p)) {
-            const int st = j % KV_STAGES;
-            const uint32_t ph = ((j / KV_STAGES) & 1) ^ 1;
-            const TileRef tr = cur.ref(p);
-            const int bits = MIXED ? p.ranges.r[tr.g].bits : 4;
-            const int s0 = k % SL::STAGES, s1 = (k + stages_of(bits) - 1) % SL::STAGES;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(&stg_full[s0], (k / SL::STAGES) & 1, abort_flag, &g_err_attn)))
-                break;
-            if (bits == 8 && !__all_sync(0xffffffffu, mbar_wait(&stg_full[s1], ((k + 1) / SL::STAGES) & 1,
-                                                                abort_flag, &g_err_attn)))
-                break;
-            const uint8_t *stg_k = sStg + s0 * SL::STAGE_BYTES;
-            const uint8_t *stg_v = bits == 8 ? sStg + s1 * SL::STAGE_BYTES : stg_k + SL::INT4_V_OFFSET;
-            uint8_t *kt = sK + st * K_TILE_BYTES;
-            uint8_t *vt = sV + st * V_TILE_BYTES;
-            const bool fine = (!MIXED || bits == 4)
-                                  ? decode_tile<4>(stg_k, stg_v, d, tr.valid, rank, sc, kt, vt, &k_empty[st],
-                                                   &v_empty[st], ph, abort_flag)
-                                  : decode_tile<8>(stg_k, stg_v, d, tr.valid, rank, sc, kt, vt, &k_empty[st],
-                                                   &v_empty[st], ph, abort_flag);
-            if (!fine) break;
-            mbar_arrive(&stg_empty[s0]);  // every staged byte of this tile has been read
-            if (bits == 8) mbar_arrive(&stg_empty[s1]);
-            k += stages_of(bits);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&kv_full[st]), 0));
-            if (j + 1 < T) prefetch_scales();
+        int j = 0;
+        bool going = ok;
+        // Tiles go in stretches of one precision, each through a loop compiled for it,
+        // so an INT4 stretch runs the same code as the INT4-only kernel.
+        auto stretch = [&](auto bits_c) {
+            constexpr int BITS = decltype(bits_c)::value;
+            const int g0 = cur.g;
+            for (; j < T && (!MIXED || cur.g == g0); ++j, cur.next(p)) {
+                const int st = j % KV_STAGES;
+                const uint32_t ph = ((j / KV_STAGES) & 1) ^ 1;
+                const TileRef tr = cur.ref(p);
+                const int s0 = k % SL::STAGES, s1 = (k + stages_of(BITS) - 1) % SL::STAGES;
+                if (*abort_flag ||
+                    !__all_sync(0xffffffffu, mbar_wait(&stg_full[s0], (k / SL::STAGES) & 1, abort_flag, &g_err_attn)) ||
+                    (BITS == 8 && !__all_sync(0xffffffffu, mbar_wait(&stg_full[s1], ((k + 1) / SL::STAGES) & 1,
+                                                                     abort_flag, &g_err_attn)))) {
+                    going = false;
+                    return;
+                }
+                const uint8_t *stg_k = sStg + s0 * SL::STAGE_BYTES;
+                const uint8_t *stg_v = BITS == 8 ? sStg + s1 * SL::STAGE_BYTES : stg_k + SL::INT4_V_OFFSET;
+                uint8_t *kt = sK + st * K_TILE_BYTES;
+                uint8_t *vt = sV + st * V_TILE_BYTES;
+                if (!decode_tile<BITS>(stg_k, stg_v, d, tr.valid, rank, sc, kt, vt, &k_empty[st], &v_empty[st], ph,
+                                       abort_flag)) {
+                    going = false;
+                    return;
+                }
+                mbar_arrive(&stg_empty[s0]);  // every staged byte of this tile has been read
+                if (BITS == 8) mbar_arrive(&stg_empty[s1]);
+                k += stages_of(BITS);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&kv_full[st]), 0));
+                if (j + 1 < T) prefetch_scales();
+            }
+        };
+        while (going && j < T) {
+            if (!MIXED || p.ranges.r[cur.g].bits == 4) stretch(std::integral_constant<int, 4>{});
+            else stretch(std::integral_constant<int, 8>{});
         }
     }
     } else {
