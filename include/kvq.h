@@ -66,7 +66,7 @@ enum kvq_status {
     KVQ_OK = 0,
     KVQ_ERR_ARG = 1,         /* a size, count or pointer argument is invalid */
     KVQ_ERR_ALIGN = 2,       /* a pointer or leading dimension is not 16-byte aligned */
-    KVQ_ERR_UNSUPPORTED = 3, /* a valid but unsupported combination (e.g. causal) */
+    KVQ_ERR_UNSUPPORTED = 3, /* a valid but unsupported combination (a RoPE width other than 64 or 128) */
     KVQ_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
     KVQ_ERR_TIMEOUT = 5      /* a device-side wait ran out (see kvq_device_status) */
 };
