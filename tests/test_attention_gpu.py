@@ -38,7 +38,8 @@ def _assert_close(got, ref):
     return float(err.max()), float(rel)
 
 
-@pytest.mark.parametrize("n_q,n_kv,heads", [(77, 1, 2), (128, 128, 2), (256, 256, 1), (300, 129, 2), (129, 1000, 3), (513, 2000, 2)])
+@pytest.mark.parametrize("n_q,n_kv,heads", [(77, 1, 2), (1, 300, 2), (1, 1, 1), (128, 128, 2), (256, 256, 1), (300, 129, 2),
+                                         (129, 1000, 3), (513, 2000, 2)])
 def test_random_store_fp32(n_q, n_kv, heads):
     st = _store(heads, n_kv, seed=n_kv)
     q = inputs.random_q(n_q, heads * 128, seed=n_q, std=2.0).cuda()

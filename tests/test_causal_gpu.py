@@ -46,6 +46,9 @@ def _assert_close(got, ref):
     (513, 2000, 1487, 2),  # the last chunk: its last row sees every key
     (600, 700, 0, 2),      # fewer queries than keys
     (1100, 300, 0, 1),     # more queries than keys: rows past 299 see them all
+    (1, 1, 0, 1),          # one query, one key
+    (1, 700, 699, 2),      # one query at the last position: sees every key
+    (1, 700, 200, 2),      # one query in the middle
 ])
 def test_causal_matches_oracle(n_q, n_kv, q_pos0, heads):
     st = _store(heads, n_kv, seed=n_kv + q_pos0)
