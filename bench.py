@@ -567,7 +567,8 @@ def run_gpu(args, wl, world, rank, local):
                                       "query chunks, Q only recomputed, attention, output chunk back to the host; "
                                       "device_gib = packed store + chunk buffers (x, Q and output never held in "
                                       "full), W excluded as in the peak comparison"},
-            "gpu_launches": 2 * args.steps,
+            # per step: the projection (and, routed, the fine store's K/V section) and the attention calls
+            "gpu_launches": ((2 + len(routed_segs)) if route else 2) * args.steps,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
