@@ -8,21 +8,27 @@
 // `_phase1_kv` fixes the fused row layout ([q | k | v], heads of 128
 // contiguous columns) and `_norm_rope` the per-head RMSNorm of Q and K.
 //
-// Design (one CTA per SM, persistent):
-//   tile       128 tokens x 256 output columns (two heads), K-step 64
-//   warp 0     TMA producer: x tile [128 x 64] and W tile [256 x 64] per
-//              stage, 128-byte swizzle, 4-stage shared-memory ring
-//   warp 1     TMEM allocator and MMA issuer: tcgen05.mma kind::f16
-//              M=128 N=256 K=16, fp32 accumulators in TMEM, two 256-column
-//              accumulators so the epilogue of one tile overlaps the main
-//              loop of the next
-//   warps 2-5  epilogue: one thread per token row reads a head's 128 fp32
-//              values from TMEM (tcgen05.ld 32x32b), applies RMSNorm (Q, K,
-//              optional), the 128-point rotation, and writes Q as BF16 or
-//              K / V as group-scaled INT4 / INT8 codes into the head-major
-//              store.  The accumulator never leaves the SM in fp32 or BF16.
+// Design (CTA pairs on two SMs, persistent, one pair per two SMs):
+//   tile       256 tokens x 256 output columns (two heads) per pair, K-step 64;
+//              each CTA owns 128 of the tokens
+//   warp 0     TMA producer of each CTA: its 128 rows of x and its half (128
+//              rows) of the tile's W rows per stage, 128-byte swizzle,
+//              6-stage shared-memory ring
+//   warp 1     TMEM allocation (jointly with the peer).  In the even CTA the
+//              MMA issuer: tcgen05.mma.cta_group::2 kind::f16 M=256 N=256
+//              K=16 (rows 0-127 from the even CTA, 128-255 from the odd one;
+//              B split along N between the two SMs), fp32 accumulators in each
+//              CTA's TMEM, two 256-column accumulators so the epilogue of one
+//              tile overlaps the main loop of the next.  In the odd CTA it
+//              relays each of its landed stages to the even CTA's barrier.
+//   warps 2-5  epilogue of each CTA on its own 128 rows: one thread per token
+//              row reads a head's 128 fp32 values from TMEM (tcgen05.ld
+//              32x32b), applies RMSNorm (Q, K, optional), the 128-point
+//              rotation, and writes Q as BF16 or K / V as group-scaled INT4 /
+//              INT8 codes into the head-major store.  The accumulator never
+//              leaves the SM in fp32 or BF16.
 // Tiles are walked chunk by chunk (chunk_tokens rows at a time, rounded up
-// to whole 128-row tiles), columns-outer within a chunk, so that a chunk of
+// to whole 256-row pair tiles), columns-outer within a chunk, so that a chunk of
 // x and a few W column blocks stay in L2.  Every output element depends only
 // on its token row, so the results do not depend on the chunk size.
 #include <cuda.h>
@@ -38,9 +44,11 @@ namespace {
 
 __device__ unsigned int g_err_proj;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6;
+constexpr int BNH = BN / 2;          // W rows (output columns) each CTA of the pair loads
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
+constexpr int B_BYTES = BNH * BK * 2;
+constexpr uint16_t kPairMask = 0x3;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
@@ -62,6 +70,7 @@ struct ProjParams {
     RangeTable ranges;
 };
 
+// m_idx counts pair tiles of 2 * BM rows (p.m_tiles, p.chunk_m_tiles are in pair tiles)
 __device__ __forceinline__ void tile_coords(int64_t T, const ProjParams &p, int &m_idx, int &n_idx) {
     const int64_t per_chunk = static_cast<int64_t>(p.chunk_m_tiles) * p.n_tiles;
     const int64_t c = T / per_chunk;
@@ -127,29 +136,33 @@ __device__ __forceinline__ void store_codes(const float (&v)[128], uint8_t *code
 }
 
 template <int GROUP, int ROT>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     qkv_proj_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ ProjParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *smem_a = smem;
     uint8_t *smem_b = smem + STAGES * A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-    uint64_t *empty = full + STAGES;
-    uint64_t *tfull = empty + STAGES;
-    uint64_t *tempty = tfull + 2;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);  // this CTA's copies landed
+    uint64_t *peer_full = full + STAGES;  // even CTA: the odd CTA's copies landed
+    uint64_t *empty = peer_full + STAGES;  // both CTAs: the stage's MMAs completed
+    uint64_t *tfull = empty + STAGES;      // both CTAs: an accumulator is complete
+    uint64_t *tempty = tfull + 2;          // even CTA: both CTAs' epilogues have read an accumulator
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
+            mbar_init(&peer_full[i], 1);
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 128);
+            mbar_init(&tempty[i], 2 * 4);  // one arrive per epilogue warp of both CTAs
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -159,29 +172,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tmap(&tm_w);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
     }
+    // the peer may arrive on this CTA's barriers only once they are initialised
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------- TMA producer (both CTAs)
+        // its 128 rows of x and its half (128 rows) of the tile's W rows, into its own ring
         if (elect_one()) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0;  // bit s: stage s has been armed at least once
             uint32_t armed_parity = 0;
-            for (int64_t T = blockIdx.x; T < p.total_tiles && !*abort_flag; T += gridDim.x) {
+            for (int64_t T = cluster; T < p.total_tiles && !*abort_flag; T += clusters) {
                 int m_idx, n_idx;
                 tile_coords(T, p, m_idx, n_idx);
+                const int y = (2 * m_idx + static_cast<int>(rank)) * BM;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_err_proj)) break;
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_2d(smem_a + stage * A_BYTES, &tm_x, &full[stage], kb * BK, m_idx * BM);
-                    tma_load_2d(smem_b + stage * B_BYTES, &tm_w, &full[stage], kb * BK, n_idx * BN);
+                    tma_load_2d(smem_a + stage * A_BYTES, &tm_x, &full[stage], kb * BK, y);
+                    tma_load_2d(smem_b + stage * B_BYTES, &tm_w, &full[stage], kb * BK,
+                                n_idx * BN + static_cast<int>(rank) * BNH);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -197,21 +214,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        if (elect_one()) {
-            constexpr uint32_t idesc = make_idesc_f16(BM, BN, 1);
+        if (rank == 1) {
+            // ------------------------------------------------------ odd CTA: relay of its landed stages
+            if (elect_one()) {
+                const uint32_t peer = mapa_shared(smem_u32(peer_full), 0);
+                int stage = 0;
+                uint32_t phase = 0;
+                for (int64_t T = cluster; T < p.total_tiles && !*abort_flag; T += clusters) {
+                    bool ok = true;
+                    for (int kb = 0; kb < p.k_blocks; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, abort_flag, &g_err_proj)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_cluster(peer + stage * 8);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                }
+            }
+        } else if (elect_one()) {
+            // ------------------------------------------------------ even CTA: MMA issuer for the pair
+            constexpr uint32_t idesc = make_idesc_f16(2 * BM, BN, 1);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool issued = false;
-            for (int64_t T = blockIdx.x; T < p.total_tiles && !*abort_flag; T += gridDim.x) {
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, &g_err_proj)) break;
+            for (int64_t T = cluster; T < p.total_tiles && !*abort_flag; T += clusters) {
+                if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, &g_err_proj)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 bool ok = true;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, &g_err_proj)) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, &g_err_proj) ||
+                        !mbar_wait_cluster(&peer_full[stage], phase, abort_flag, &g_err_proj)) {
                         ok = false;
                         break;
                     }
@@ -220,27 +260,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t b_addr = smem_u32(smem_b + stage * B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        mma_f16_ss(d_tmem, make_sdesc_sw128(a_addr + k * 32), make_sdesc_sw128(b_addr + k * 32),
-                                   idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_f16_ss_pair(d_tmem, make_sdesc_sw128(a_addr + k * 32), make_sdesc_sw128(b_addr + k * 32),
+                                        idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     issued = true;
-                    mma_commit(&empty[stage]);
+                    mma_commit_pair(&empty[stage], kPairMask);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(&tfull[acc]);
+                mma_commit_pair(&tfull[acc], kPairMask);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (issued && *abort_flag) {
-                // drain: wait until every MMA issued so far has completed
+                // drain: every MMA issued so far has completed before the pair tears down
                 volatile int no_abort = 0;
                 uint64_t *drain = &tfull[acc];
-                mma_commit(drain);
-                mbar_wait(drain, acc_phase, &no_abort, nullptr);
+                mma_commit_pair(drain, 0x1);
+                mbar_wait(drain, acc_phase, &no_abort, nullptr, 1000000000ull);
             }
         }
         __syncwarp();
@@ -251,9 +291,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int64_t T = blockIdx.x; T < p.total_tiles && !*abort_flag; T += gridDim.x) {
+        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        for (int64_t T = cluster; T < p.total_tiles && !*abort_flag; T += clusters) {
             int m_idx, n_idx;
             tile_coords(T, p, m_idx, n_idx);
+            m_idx = 2 * m_idx + static_cast<int>(rank);  // this CTA's 128-row tile of the pair's 256
             // warp-uniform before the warp-collective TMEM loads
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_err_proj))) break;
             tc_fence_after();
@@ -322,16 +364,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader + acc * 8);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
 
+    // neither CTA of the pair frees TMEM or leaves while the other may still touch its memory
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 }  // namespace
@@ -362,19 +406,19 @@ int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int gro
                        static_cast<uint64_t>(hidden) * 2, BK, BM))
         return KVQ_ERR_CUDA;
     if (encode_tmap_2d(&tm_w, w, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(3) * hidden,
-                       static_cast<uint64_t>(hidden) * 2, BK, BN))
+                       static_cast<uint64_t>(hidden) * 2, BK, BNH))
         return KVQ_ERR_CUDA;
     ProjParams p{};
     p.n = n;
     p.hidden = hidden;
-    p.m_tiles = static_cast<int>((n + BM - 1) / BM);
+    p.m_tiles = static_cast<int>((n + 2 * BM - 1) / (2 * BM));  // pair tiles of 256 rows
     // the W rows (output columns) of the requested sections: Q = [0, C), K and V = [C, 3C)
     const int c0 = (sections & 1) ? 0 : hidden, c1 = (sections & 2) ? 3 * hidden : hidden;
     p.col_tile0 = c0 / BN;
     p.n_tiles = (c1 + BN - 1) / BN - p.col_tile0;
     p.sections = sections;
     p.k_blocks = hidden / BK;
-    int64_t cm = chunk_tokens <= 0 ? p.m_tiles : (chunk_tokens + BM - 1) / BM;
+    int64_t cm = chunk_tokens <= 0 ? p.m_tiles : (chunk_tokens + 2 * BM - 1) / (2 * BM);
     if (cm > p.m_tiles) cm = p.m_tiles;
     p.chunk_m_tiles = static_cast<int>(cm);
     p.total_tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -385,7 +429,8 @@ int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int gro
     p.ranges = ranges;
     p.rope_cs = rope_cs;
     const int rot = rope_cs ? rot_dim : 0;
-    const int grid = static_cast<int>(p.total_tiles < sm_count() ? p.total_tiles : sm_count());
+    const int64_t pairs = sm_count() / 2;  // one CTA pair per two SMs, persistent
+    const int grid = 2 * static_cast<int>(p.total_tiles < pairs ? p.total_tiles : pairs);
     cudaError_t e;
     if (group == 32) e = launch_rot<32>(tm_x, tm_w, p, rot, grid, s);
     else if (group == 64) e = launch_rot<64>(tm_x, tm_w, p, rot, grid, s);
