@@ -68,13 +68,19 @@ def _load():
             lib.kvqo_kv_unpack.restype = I
             lib.kvqo_kv_unpack.argtypes = [P, P, P, P, I64, I, I, I, P]
             lib.kvqo_qkv_proj.restype = I
-            lib.kvqo_qkv_proj.argtypes = [P, P, I, P, I64, I, I, P, P, F, P, I, P, P, P, P, P, P]
+            lib.kvqo_qkv_proj.argtypes = [P, P, I, P, I64, I, I, P, P, F, P, I, P, P, P, P, P, P, P, P]
             lib.kvqo_attention.restype = I
             lib.kvqo_attention.argtypes = [P, I64, I, P, P, P, P, I64, I64, I, I, F, P, I64, P]
             lib.kvqo_attention_causal.restype = I
             lib.kvqo_attention_causal.argtypes = [P, I64, I, P, P, P, P, I64, I64, I, I, F, I64, P, I64, P]
             lib.kvqo_attention_mixed.restype = I
             lib.kvqo_attention_mixed.argtypes = [P, I64, I, I, P, P, P, P, P, P, P, P, I, F, P, I64, P]
+            lib.kvqo_attention_partial.restype = I
+            lib.kvqo_attention_partial.argtypes = [P, I64, I, I, P, P, P, P, P, P, P, P, I, F, P, I64, P, P]
+            lib.kvqo_lse_merge.restype = None
+            lib.kvqo_lse_merge.argtypes = [P, P, P, P, I64]
+            lib.kvqo_partial_finish.restype = None
+            lib.kvqo_partial_finish.argtypes = [P, I64, P]
             lib.kvqo_threads.restype = I
             lib.kvqo_threads.argtypes = []
             _lib = lib
@@ -186,9 +192,10 @@ def kv_unpack(kc, vc, ks, vs, *, group: int = 32, bits: int = 4) -> np.ndarray:
 def qkv_proj(x, w, rows=None, *, group: int = 32, bits: int = 4, q_norm_w=None, k_norm_w=None, eps: float = 1e-6,
              rope_cs=None):
     """x: uint16 BF16 bits [n, C]; w: uint16 BF16 bits [3C, C].  Returns a dict
-    with q_f32 [n_rows, C], q_bf16 [n_rows, C] (uint16) and compact
-    token-major k_codes, v_codes, k_scales, v_scales for `rows`.  rope_cs:
-    optional fp32 [n, rot_dim/2, 2] (cos, sin) per token row for the
+    with q_f32 [n_rows, C], q_bf16 [n_rows, C] (uint16), compact token-major
+    k_codes, v_codes, k_scales, v_scales for `rows`, and k_rot / v_rot
+    [n_rows, C] fp32: the rotated K and V vectors the quantiser was given.
+    rope_cs: optional fp32 [n, rot_dim/2, 2] (cos, sin) per token row for the
     split-half RoPE of Q and K after the RMSNorm."""
     x, w = _c(x, np.uint16), _c(w, np.uint16)
     n, C = x.shape
@@ -207,10 +214,12 @@ def qkv_proj(x, w, rows=None, *, group: int = 32, bits: int = 4, q_norm_w=None, 
         v_codes=np.empty((len(rows), heads, HD * bits // 8), np.uint8),
         k_scales=np.empty((len(rows), heads, HD // group), np.uint16),
         v_scales=np.empty((len(rows), heads, HD // group), np.uint16),
+        k_rot=np.empty((len(rows), C), np.float32),
+        v_rot=np.empty((len(rows), C), np.float32),
     )
     rc = _load().kvqo_qkv_proj(_p(x), _p(w), C, _p(rows), len(rows), group, bits, _p(qn), _p(kn), eps, _p(rc_), rot,
                                _p(out["q_f32"]), _p(out["q_bf16"]), _p(out["k_codes"]), _p(out["v_codes"]),
-                               _p(out["k_scales"]), _p(out["v_scales"]))
+                               _p(out["k_scales"]), _p(out["v_scales"]), _p(out["k_rot"]), _p(out["v_rot"]))
     if rc:
         raise ValueError("oracle qkv_proj: bad arguments")
     return out
@@ -260,6 +269,30 @@ def attention_causal(q, k_codes, v_codes, k_scales, v_scales, *, n_kv: int, q_po
     return out
 
 
+class _RangeArgs:
+    """A range table marshalled for the C oracle (keeps the arrays alive)."""
+
+    def __init__(self, ranges):
+        self.keep = []
+        self.arrs = {}
+        for key, dt in (("k_codes", np.uint8), ("v_codes", np.uint8), ("k_scales", np.uint16),
+                        ("v_scales", np.uint16)):
+            lst = [_c(r[key], dt) for r in ranges]
+            ptrs = (ctypes.c_void_p * len(lst))(*[a.ctypes.data for a in lst])
+            self.keep += lst + [ptrs]
+            self.arrs[key] = ctypes.cast(ptrs, ctypes.c_void_p)
+        self.n = len(ranges)
+        self.starts = np.array([r["start"] for r in ranges], np.int64)
+        self.lens = np.array([r["len"] for r in ranges], np.int64)
+        self.bitss = np.array([r["bits"] for r in ranges], np.int32)
+        self.caps = np.array([_c(r["k_codes"], np.uint8).shape[1] for r in ranges], np.int64)
+
+    def args(self):
+        a = self.arrs
+        return (self.n, _p(self.starts), _p(self.lens), _p(self.bitss), _p(self.caps), a["k_codes"], a["v_codes"],
+                a["k_scales"], a["v_scales"])
+
+
 def attention_mixed(q, ranges, *, group: int = 32, sm_scale: float | None = None, rows=None) -> np.ndarray:
     """ranges: list of dicts with start, len, bits and the range's own
     head-major store (k_codes, v_codes, k_scales, v_scales; capacity = their
@@ -269,21 +302,61 @@ def attention_mixed(q, ranges, *, group: int = 32, sm_scale: float | None = None
     heads = C // HD
     rows = np.arange(n_q, dtype=np.int64) if rows is None else _c(rows, np.int64)
     sm = HD ** -0.5 if sm_scale is None else sm_scale
-    keep = []
-    arrs = {}
-    for key, dt in (("k_codes", np.uint8), ("v_codes", np.uint8), ("k_scales", np.uint16), ("v_scales", np.uint16)):
-        lst = [_c(r[key], dt) for r in ranges]
-        ptrs = (ctypes.c_void_p * len(lst))(*[a.ctypes.data for a in lst])
-        keep += lst + [ptrs]
-        arrs[key] = ctypes.cast(ptrs, ctypes.c_void_p)
-    starts = np.array([r["start"] for r in ranges], np.int64)
-    lens = np.array([r["len"] for r in ranges], np.int64)
-    bitss = np.array([r["bits"] for r in ranges], np.int32)
-    caps = np.array([_c(r["k_codes"], np.uint8).shape[1] for r in ranges], np.int64)
+    ra = _RangeArgs(ranges)
     out = np.empty((len(rows), C), np.float32)
-    rc = _load().kvqo_attention_mixed(_p(q), C, heads, len(ranges), _p(starts), _p(lens), _p(bitss), _p(caps),
-                                      arrs["k_codes"], arrs["v_codes"], arrs["k_scales"], arrs["v_scales"],
-                                      group, sm, _p(rows), len(rows), _p(out))
+    rc = _load().kvqo_attention_mixed(_p(q), C, heads, *ra.args(), group, sm, _p(rows), len(rows), _p(out))
     if rc:
         raise ValueError("oracle attention_mixed: bad arguments")
     return out
+
+
+# ----------------------------------------------------------------- next row f3: attention over key chunks
+def attention_partial(q, ranges, *, group: int = 32, sm_scale: float | None = None, rows=None):
+    """Partial attention of query rows against one key chunk (vram_lab.py's
+    blockwise attention: each K/V block's normalised output and its
+    log-sum-exp).  `ranges` as attention_mixed, tiling the chunk's keys.
+    Returns (o, lse): o fp64 [n_rows, heads, 128] in the ROTATED basis, lse fp64
+    [n_rows, heads] = log sum_j exp(s_j) over the chunk's keys."""
+    q = _c(q, np.uint16)
+    n_q, C = q.shape
+    heads = C // HD
+    rows = np.arange(n_q, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    sm = HD ** -0.5 if sm_scale is None else sm_scale
+    ra = _RangeArgs(ranges)
+    o = np.empty((len(rows), heads, HD), np.float64)
+    lse = np.empty((len(rows), heads), np.float64)
+    rc = _load().kvqo_attention_partial(_p(q), C, heads, *ra.args(), group, sm, _p(rows), len(rows), _p(o), _p(lse))
+    if rc:
+        raise ValueError("oracle attention_partial: bad arguments")
+    return o, lse
+
+
+def lse_merge(o_a, lse_a, o_b, lse_b):
+    """vram_lab.py `_online_combine` of two partials over disjoint key sets;
+    returns the merged (o, lse) as new arrays."""
+    o = _c(o_a, np.float64).copy()
+    lse = _c(lse_a, np.float64).copy()
+    ob, lb = _c(o_b, np.float64), _c(lse_b, np.float64)
+    assert o.shape == ob.shape and lse.shape == lb.shape and o.shape[:-1] == lse.shape and o.shape[-1] == HD
+    _load().kvqo_lse_merge(_p(o), _p(lse), _p(ob), _p(lb), lse.size)
+    return o, lse
+
+
+def partial_finish(o) -> np.ndarray:
+    """Merged o [n_rows, heads, 128] (rotated) -> fp32 output [n_rows, heads*128],
+    rounded to fp32 and un-rotated."""
+    o = _c(o, np.float64)
+    out = np.empty(o.shape, np.float32)
+    _load().kvqo_partial_finish(_p(o), o.size // HD, _p(out))
+    return out.reshape(o.shape[0], -1)
+
+
+def attention_blockwise(q, chunks, *, group: int = 32, sm_scale: float | None = None, rows=None) -> np.ndarray:
+    """Attention over a sequence of key chunks (each a range table, as
+    attention_partial), merged in the given order and un-rotated once at the
+    end: vram_lab.py's `_blockwise_attention_q` on the packed store."""
+    o = lse = None
+    for ch in chunks:
+        ob, lb = attention_partial(q, ch, group=group, sm_scale=sm_scale, rows=rows)
+        o, lse = (ob, lb) if o is None else lse_merge(o, lse, ob, lb)
+    return partial_finish(o)

@@ -286,11 +286,14 @@ static void rope_split_half(float *v, const float *cs, int rot_dim) {
  * q_bf16.  K: optional RMSNorm (k_norm_w) -> optional RoPE -> rotate -> quantise.
  * V: rotate -> quantise.  The rotation and quantiser take the fp32
  * accumulator, with no BF16 rounding in between.  Outputs compact token-major
- * as in kvqo_kv_rotate_quant_pack; q_f32 / q_bf16 are [n_rows][C]. */
+ * as in kvqo_kv_rotate_quant_pack; q_f32 / q_bf16 are [n_rows][C].  k_rot and
+ * v_rot (optional, [n_rows][C] fp32) receive the rotated K and V vectors that
+ * the quantiser is given, so a caller can see how close each code and scale
+ * sits to a rounding boundary. */
 int kvqo_qkv_proj(const uint16_t *x, const uint16_t *w, int hidden, const int64_t *rows, int64_t n_rows, int group,
                   int bits, const float *q_norm_w, const float *k_norm_w, float eps, const float *rope_cs, int rot_dim,
                   float *q_f32, uint16_t *q_bf16, uint8_t *k_codes, uint8_t *v_codes, uint16_t *k_scales,
-                  uint16_t *v_scales) {
+                  uint16_t *v_scales, float *k_rot, float *v_rot) {
     if (check_fmt(hidden, group, bits)) return 1;
     if (rope_cs && (rot_dim < 2 || rot_dim > HD || rot_dim % 2)) return 1;
     const int C = hidden, heads = C / HD, cb = HD * bits / 8, sg = HD / group;
@@ -319,8 +322,10 @@ int kvqo_qkv_proj(const uint16_t *x, const uint16_t *w, int hidden, const int64_
             if (k_norm_w) rmsnorm128(kk, k_norm_w, eps);
             if (rope_cs) rope_split_half(kk, rope_cs + rows[r] * rot_dim, rot_dim);
             kvqo_rotate128(kk, y);
+            if (k_rot) memcpy(k_rot + r * C + h * HD, y, sizeof(y));
             kvqo_quant_head(y, group, bits, k_codes + (r * heads + h) * cb, k_scales + (r * heads + h) * sg);
             kvqo_rotate128(vv, y);
+            if (v_rot) memcpy(v_rot + r * C + h * HD, y, sizeof(y));
             kvqo_quant_head(y, group, bits, v_codes + (r * heads + h) * cb, v_scales + (r * heads + h) * sg);
         }
         free(xf);
@@ -501,6 +506,120 @@ int kvqo_attention_mixed(const uint16_t *q, int64_t ldq, int heads, int n_ranges
     free(Kd);
     free(Vd);
     return 0;
+}
+
+/* ------------------------------------------------------------------ next row f3: attention over key chunks */
+
+/* One query row and head against one chunk of keys ([V] `_blockwise_attention`
+ * and `_blockwise_attention_q`: each K/V block gives a partial result and its
+ * log-sum-exp, later merged by `_online_combine`).  In the rotated basis, with
+ * s_j = (q . k^_j) * sm_scale over the chunk's keys:
+ *   o   = sum_j exp(s_j - m) v^_j / sum_j exp(s_j - m),   m = max_j s_j
+ *   lse = m + log(sum_j exp(s_j - m))      (= log sum_j exp(s_j))
+ * o is NOT un-rotated (the merge works in the rotated basis, and the single
+ * un-rotation comes at the end).  fp64 throughout. */
+static void partial_head(const float *qf, const float *Kd, const float *Vd, int64_t n_kv, float sm_scale, double *o,
+                         double *lse, double *p) {
+    double m = -HUGE_VAL;
+    for (int64_t j = 0; j < n_kv; ++j) {
+        const float *k = Kd + j * HD;
+        double s = 0.0;
+        for (int d = 0; d < HD; ++d) s += (double)qf[d] * (double)k[d];
+        s *= (double)sm_scale;
+        p[j] = s;
+        if (s > m) m = s;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n_kv; ++j) {
+        p[j] = exp(p[j] - m);
+        l += p[j];
+    }
+    for (int d = 0; d < HD; ++d) o[d] = 0.0;
+    for (int64_t j = 0; j < n_kv; ++j) {
+        const float *v = Vd + j * HD;
+        for (int d = 0; d < HD; ++d) o[d] += p[j] * (double)v[d];
+    }
+    for (int d = 0; d < HD; ++d) o[d] /= l;
+    *lse = m + log(l);
+}
+
+/* Partial attention of the listed query rows against one key chunk given as a
+ * range table (layout and arguments as kvqo_attention_mixed).  Outputs, fp64:
+ *   o_out   [n_rows][heads][128]  normalised output in the rotated basis
+ *   lse_out [n_rows][heads]       natural log of sum_j exp(s_j) over the chunk */
+int kvqo_attention_partial(const uint16_t *q, int64_t ldq, int heads, int n_ranges, const int64_t *starts,
+                           const int64_t *lens, const int *bitss, const int64_t *caps, const uint8_t *const *k_codes,
+                           const uint8_t *const *v_codes, const uint16_t *const *k_scales,
+                           const uint16_t *const *v_scales, int group, float sm_scale, const int64_t *rows,
+                           int64_t n_rows, double *o_out, double *lse_out) {
+    int64_t n_kv = 0;
+    for (int g = 0; g < n_ranges; ++g) {
+        if (check_fmt(heads * HD, group, bitss[g]) || lens[g] < 1 || caps[g] < lens[g] || starts[g] != n_kv) return 1;
+        n_kv += lens[g];
+    }
+    if (n_kv < 1) return 1;
+    const int sg = HD / group;
+    float *Kd = (float *)malloc(sizeof(float) * (size_t)n_kv * HD);
+    float *Vd = (float *)malloc(sizeof(float) * (size_t)n_kv * HD);
+    if (!Kd || !Vd) {
+        free(Kd);
+        free(Vd);
+        return 2;
+    }
+    for (int h = 0; h < heads; ++h) {
+        for (int g = 0; g < n_ranges; ++g) {
+            const int cb = HD * bitss[g] / 8;
+#pragma omp parallel for schedule(static)
+            for (int64_t j = 0; j < lens[g]; ++j) {
+                int64_t t = (int64_t)h * caps[g] + j;
+                kvqo_dequant_head(k_codes[g] + t * cb, k_scales[g] + t * sg, group, bitss[g], Kd + (starts[g] + j) * HD);
+                kvqo_dequant_head(v_codes[g] + t * cb, v_scales[g] + t * sg, group, bitss[g], Vd + (starts[g] + j) * HD);
+            }
+        }
+#pragma omp parallel
+        {
+            double *p = (double *)malloc(sizeof(double) * (size_t)n_kv);
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < n_rows; ++r) {
+                float qf[HD];
+                for (int d = 0; d < HD; ++d) qf[d] = kvqo_bf16_to_f32(q[rows[r] * ldq + h * HD + d]);
+                partial_head(qf, Kd, Vd, n_kv, sm_scale, o_out + (r * heads + h) * HD, lse_out + r * heads + h, p);
+            }
+            free(p);
+        }
+    }
+    free(Kd);
+    free(Vd);
+    return 0;
+}
+
+/* log(exp(a) + exp(b)), computed from the larger argument. */
+static double log_add_exp(double a, double b) {
+    const double hi = a > b ? a : b, lo = a > b ? b : a;
+    return hi + log1p(exp(lo - hi));
+}
+
+/* Merge of two partial results over disjoint key sets ([V] `_online_combine`):
+ *   new = log(exp(lse_a) + exp(lse_b))
+ *   o   = o_a * exp(lse_a - new) + o_b * exp(lse_b - new)
+ * written into (o_a, lse_a).  n_vec vectors of 128, one lse each; fp64. */
+void kvqo_lse_merge(double *o_a, double *lse_a, const double *o_b, const double *lse_b, int64_t n_vec) {
+    for (int64_t i = 0; i < n_vec; ++i) {
+        const double nw = log_add_exp(lse_a[i], lse_b[i]);
+        const double wa = exp(lse_a[i] - nw), wb = exp(lse_b[i] - nw);
+        for (int d = 0; d < HD; ++d) o_a[i * HD + d] = o_a[i * HD + d] * wa + o_b[i * HD + d] * wb;
+        lse_a[i] = nw;
+    }
+}
+
+/* The end of the chunked attention: each merged vector rounded to fp32 and
+ * un-rotated once (the rotation of the format; H^T = H). */
+void kvqo_partial_finish(const double *o, int64_t n_vec, float *out) {
+    for (int64_t i = 0; i < n_vec; ++i) {
+        float of[HD];
+        for (int d = 0; d < HD; ++d) of[d] = (float)o[i * HD + d];
+        kvqo_rotate128(of, out + i * HD);
+    }
 }
 
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */

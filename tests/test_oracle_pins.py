@@ -538,3 +538,120 @@ def test_attention_mixed_equals_concatenated_store():
             np.stack([oracle.dequant_head(b[1][h, j], b[3].view(np.uint16)[h, j], 32, 4) for j in range(70)])])
         P = scipy.special.softmax(qf[:, h] @ K.astype(np.float64).T / np.sqrt(HD), axis=-1)
         assert np.allclose(got[:, h * HD:(h + 1) * HD], (P @ V) @ H.T, atol=1e-5)
+
+
+# ------------------------------------------------------------------ next row f3: attention over key chunks
+def _deq_np(codes, scales, group, bits):
+    v = _unpack_nibbles(codes) if bits == 4 else codes.view(np.int8).astype(np.int16)
+    return v.astype(np.float64) * np.repeat(scales.view(np.float16).astype(np.float64), group, axis=-1)
+
+
+def _chunk_ranges(stores, lens):
+    """Range table of one key chunk: consecutive ranges over the given stores
+    (each a head-major (kc, vc, ks, vs, bits) tuple) with the given lengths."""
+    out, start = [], 0
+    for (kc, vc, ks, vs, bits), ln in zip(stores, lens):
+        out.append(dict(start=start, len=ln, bits=bits, k_codes=kc, v_codes=vc, k_scales=ks.view(np.uint16),
+                        v_scales=vs.view(np.uint16)))
+        start += ln
+    return out
+
+
+def _store_np(heads, n, cap, group, bits, seed):
+    from serving_tcgen05_streamed_gb300 import inputs
+    kc, vc, ks, vs = [t.numpy() for t in inputs.random_packed_kv(heads, n, cap, group, bits, seed=seed)]
+    return kc, vc, ks.view(np.uint16), vs.view(np.uint16), bits
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_attention_partial_matches_brute_force_logsumexp(bits):
+    # o = softmax-weighted dequantised V in the rotated basis, lse = log sum exp(s):
+    # against numpy unpacking, scipy.special.softmax and scipy.special.logsumexp
+    from serving_tcgen05_streamed_gb300 import inputs
+    heads, n, nq = 2, 150, 11
+    st = _store_np(heads, n, 256, 32, bits, seed=31)
+    q = _bf16_bits(inputs.random_q(nq, heads * HD, seed=32, std=2.0))
+    o, lse = oracle.attention_partial(q, _chunk_ranges([st], [n]))
+    qf = oracle.bf16_to_f32(q).astype(np.float64).reshape(nq, heads, HD)
+    for h in range(heads):
+        K = _deq_np(st[0][h, :n], st[2][h, :n], 32, bits)
+        V = _deq_np(st[1][h, :n], st[3][h, :n], 32, bits)
+        s = qf[:, h] @ K.T * float(np.float32(HD ** -0.5))  # the scale crosses the C boundary as fp32
+        assert np.allclose(lse[:, h], scipy.special.logsumexp(s, axis=-1), rtol=0, atol=1e-10)
+        assert np.allclose(o[:, h], scipy.special.softmax(s, axis=-1) @ V, rtol=0, atol=1e-10)
+
+
+def test_lse_merge_of_disjoint_chunks_is_the_partial_of_their_union():
+    # _online_combine: merging the partials of two disjoint key sets gives the
+    # partial of the union; a wrong weight sign or a missing term fails this
+    from serving_tcgen05_streamed_gb300 import inputs
+    heads, nq = 2, 7
+    a = _store_np(heads, 60, 128, 32, 8, seed=33)
+    b = _store_np(heads, 90, 128, 32, 4, seed=34)
+    q = _bf16_bits(inputs.random_q(nq, heads * HD, seed=35, std=3.0))
+    oa, la = oracle.attention_partial(q, _chunk_ranges([a], [60]))
+    ob, lb = oracle.attention_partial(q, _chunk_ranges([b], [90]))
+    ou, lu = oracle.attention_partial(q, _chunk_ranges([a, b], [60, 90]))
+    om, lm = oracle.lse_merge(oa, la, ob, lb)
+    assert np.allclose(lm, lu, rtol=0, atol=1e-12)
+    assert np.allclose(om, ou, rtol=0, atol=1e-12)
+    # the merge is symmetric and leaves its inputs untouched
+    om2, lm2 = oracle.lse_merge(ob, lb, oa, la)
+    assert np.allclose(om2, om, rtol=0, atol=1e-14) and np.allclose(lm2, lm, rtol=0, atol=1e-14)
+    assert np.array_equal(oa, oracle.attention_partial(q, _chunk_ranges([a], [60]))[0])
+    # the log-sum-exp of the union: log(e^la + e^lb), from numpy's own logaddexp
+    assert np.allclose(lm, np.logaddexp(la, lb), rtol=0, atol=1e-12)
+
+
+def test_lse_merge_limits():
+    # a chunk whose log-sum-exp is far below the other's contributes nothing;
+    # two equal partials merge to the same output with lse + log 2
+    r = _rng(36)
+    o = r.standard_normal((3, 2, HD))
+    lse = r.standard_normal((3, 2))
+    o2 = r.standard_normal((3, 2, HD))
+    om, lm = oracle.lse_merge(o, lse, o2, lse - 800.0)
+    assert np.array_equal(om, o) and np.array_equal(lm, lse)
+    om, lm = oracle.lse_merge(o, lse, o, lse)
+    assert np.allclose(om, o, rtol=0, atol=1e-14) and np.allclose(lm, lse + np.log(2.0), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("splits", [[200], [1, 199], [128, 72], [50, 50, 50, 50], [127, 1, 72]])
+def test_blockwise_attention_equals_one_call_attention(splits):
+    # any key chunking, merged in order and un-rotated once, is the attention
+    # over all keys (exact in exact arithmetic; fp32 output rounding here).  A
+    # single chunk gives the one-call oracle's bits: same sums, one rounding.
+    from serving_tcgen05_streamed_gb300 import inputs
+    heads, n, nq = 2, 200, 9
+    kc, vc, ks, vs, _ = _store_np(heads, n, 256, 32, 4, seed=37)
+    q = _bf16_bits(inputs.random_q(nq, heads * HD, seed=38, std=2.0))
+    full = oracle.attention(q, kc, vc, ks, vs, n_kv=n)
+    chunks, a = [], 0
+    for ln in splits:  # each chunk a window of rows [a, a+ln) of the one store
+        chunks.append(_chunk_ranges([(kc[:, a:], vc[:, a:], ks[:, a:], vs[:, a:], 4)], [ln]))
+        a += ln
+    got = oracle.attention_blockwise(q, chunks)
+    if len(splits) == 1:
+        assert np.array_equal(got, full)
+    else:
+        assert np.max(np.abs(got - full)) < 2e-6 * max(1.0, np.abs(full).max())
+
+
+def test_qkv_projection_rotated_kv_outputs():
+    # k_rot / v_rot are what the quantiser sees: re-quantising them gives the
+    # stored codes and scales, and v_rot is x . W_V^T . H (library matmul)
+    r = _rng(39)
+    n, C = 5, 256
+    x = oracle.f32_to_bf16(r.standard_normal((n, C)).astype(np.float32))
+    w = oracle.f32_to_bf16((r.standard_normal((3 * C, C)) / np.sqrt(C)).astype(np.float32))
+    qn = (1.0 + 0.1 * r.standard_normal(HD)).astype(np.float32)
+    ref = oracle.qkv_proj(x, w, q_norm_w=qn, k_norm_w=qn)
+    for t in range(n):
+        for h in range(C // HD):
+            for rot, cn, sn in (("k_rot", "k_codes", "k_scales"), ("v_rot", "v_codes", "v_scales")):
+                codes, scales = oracle.quant_head(ref[rot][t, h * HD:(h + 1) * HD], 32, 4)
+                assert np.array_equal(codes, ref[cn][t, h]) and np.array_equal(scales, ref[sn][t, h])
+    xf = oracle.bf16_to_f32(x).astype(np.float64)
+    wf = oracle.bf16_to_f32(w).astype(np.float64)
+    v = (xf @ wf[2 * C:].T).reshape(n, C // HD, HD) @ H
+    assert np.allclose(ref["v_rot"].reshape(n, C // HD, HD), v, rtol=0, atol=1e-5 * np.abs(v).max())
