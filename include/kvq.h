@@ -214,6 +214,46 @@ KVQ_API int streamed_qkv_proj_ex(const void *x, const void *w_qkv, int64_t n, in
 KVQ_API int packed_kv_attention_mixed(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges, int hidden,
                               int group, float sm_scale, int out_fp32, void *out, kvq_stream_t stream);
 
+/* ---------------------------------------------------------------- next row f3: attention over key chunks
+ * vram_lab.py ("VRAM Lab"), `_blockwise_attention_q` and `_online_combine`:
+ * attention of a query chunk against K/V blocks, each block's normalised
+ * output and log-sum-exp merged into an fp32 accumulator, the output
+ * un-rotated once at the end; and the module notes on the streamed block,
+ * which plan K/V staged in host memory and streamed to the device block by
+ * block.  This call attends ONE key chunk of a packed store and carries the
+ * state between calls, so the store never needs to be on the device whole.
+ *
+ * q, n_q, hidden, group, sm_scale: as packed_kv_attention.  ranges /
+ * n_ranges: the key chunk as a range table (as packed_kv_attention_mixed; a
+ * window of a larger store is a range whose pointers start at the window's
+ * first row and whose cap is the store's head stride; starts tile [0, chunk)).
+ * The carried state, caller-owned, fp32, 16-byte aligned, not aliasing q or out:
+ *   o_acc   [n_q][hidden]  normalised output over the keys seen so far, in the
+ *                          rotated basis (not un-rotated)
+ *   lse_acc [n_q][heads]   natural log of sum_j exp(s_j) over those keys,
+ *                          s_j = sm_scale * q . k^_j
+ * flags:
+ *   0                  start: the state becomes this chunk's (o, lse)
+ *   KVQ_PARTIAL_MERGE  merge this chunk into the state:
+ *                        new = log(exp(lse_acc) + exp(lse)),
+ *                        o_acc = o_acc exp(lse_acc - new) + o exp(lse - new)
+ *   | KVQ_PARTIAL_FINAL  write the (merged) result, un-rotated, to out
+ *                      ([n_q][hidden], BF16 or fp32 by out_fp32); out may
+ *                      equal q for BF16 output.  Without FINAL, out is unused.
+ * FINAL | MERGE merges through o_acc, whose contents are unspecified after
+ * the call (lse_acc is left as it was).  FINAL alone touches no state, so
+ * o_acc / lse_acc may be NULL then (it is packed_kv_attention_mixed).
+ * Each row's result depends only on its own query row and on the order of
+ * the chunks, never on how the queries are chunked.
+ * Errors: as packed_kv_attention_mixed, plus KVQ_ERR_ARG for flags outside
+ * 0..3, a state pointer the flags need that is NULL or aliases q / out, and
+ * out NULL with FINAL; KVQ_ERR_ALIGN for a state pointer not 16-byte aligned. */
+#define KVQ_PARTIAL_MERGE 1
+#define KVQ_PARTIAL_FINAL 2
+KVQ_API int packed_kv_attention_partial(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges,
+                                        int hidden, int group, float sm_scale, int flags, float *o_acc,
+                                        float *lse_acc, int out_fp32, void *out, kvq_stream_t stream);
+
 /* ---------------------------------------------------------------- device status
  * Waits for `stream`, then returns KVQ_OK, or KVQ_ERR_TIMEOUT if a bounded
  * device wait of any kernel of this library ran out since the last call

@@ -8,4 +8,5 @@ from ._lib import (  # noqa: F401
     PackedKV, codes_bytes, device_status, kv_rotate_quant_pack, kv_unpack, load, packed_kv_attention,
     packed_kv_attention_causal, packed_kv_attention_mixed, padded_rows, scales_bytes, selftest_wait_timeout, status_str,
     streamed_qkv_proj, streamed_qkv_proj_mixed, streamed_qkv_proj_ex, SECTION_Q, SECTION_KV, version,
+    packed_kv_attention_partial, partial_state, PARTIAL_MERGE, PARTIAL_FINAL,
 )

@@ -26,7 +26,7 @@ EXPORTS = (
     "kvq_status_str", "kvq_version", "kvq_padded_rows", "kvq_codes_bytes", "kvq_scales_bytes",
     "kv_rotate_quant_pack", "kv_unpack", "streamed_qkv_proj", "packed_kv_attention",
     "packed_kv_attention_causal", "streamed_qkv_proj_mixed", "streamed_qkv_proj_ex", "packed_kv_attention_mixed",
-    "kvq_device_status",
+    "packed_kv_attention_partial", "kvq_device_status",
     "kvq_selftest_wait_timeout",
 )
 
@@ -87,6 +87,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.streamed_qkv_proj_ex.argtypes = [P, P, I64, I, I, I64, P, P, F, P, I, I, P, ctypes.POINTER(_Range), I, P]
         lib.packed_kv_attention_mixed.restype = I
         lib.packed_kv_attention_mixed.argtypes = [P, I64, ctypes.POINTER(_Range), I, I, I, F, I, P, P]
+        lib.packed_kv_attention_partial.restype = I
+        lib.packed_kv_attention_partial.argtypes = [P, I64, ctypes.POINTER(_Range), I, I, I, F, I, P, P, I, P, P]
         lib.kvq_device_status.restype = I
         lib.kvq_device_status.argtypes = [P]
         lib.kvq_selftest_wait_timeout.restype = I
@@ -329,6 +331,40 @@ def packed_kv_attention_mixed(q: torch.Tensor, stores: list[PackedKV], sm_scale:
                                           int(out_fp32), _ptr(out), _stream(stream))
     _check(st, "packed_kv_attention_mixed")
     return out
+
+
+PARTIAL_MERGE, PARTIAL_FINAL = 1, 2
+
+
+def partial_state(n_q: int, hidden: int, device="cuda"):
+    """Carried state of packed_kv_attention_partial: (o_acc fp32 [n_q, hidden],
+    lse_acc fp32 [n_q, heads])."""
+    return (torch.empty((n_q, hidden), dtype=torch.float32, device=device),
+            torch.empty((n_q, hidden // HEAD_DIM), dtype=torch.float32, device=device))
+
+
+def packed_kv_attention_partial(q: torch.Tensor, stores: list[PackedKV], state=None, merge: bool = False,
+                                final: bool = False, sm_scale: float = 0.0, out_fp32: bool = False,
+                                out: torch.Tensor | None = None, stream=None):
+    """Attention of q against ONE key chunk (`stores`: its ranges, e.g. row
+    windows of a larger store) with a carried state (o_acc, lse_acc):
+    merge=False starts the state, merge=True merges this chunk into it;
+    final=True writes the un-rotated result to `out` and returns it, otherwise
+    the state is updated and returned.  Chunks merge in call order."""
+    _need_cuda(q)
+    n_q, C = q.shape
+    if state is None:
+        state = partial_state(n_q, C, q.device) if (merge or not final) else (None, None)
+    o_acc, lse_acc = state
+    if final and out is None:
+        out = torch.empty((n_q, C), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)
+    arr = _ranges(stores)
+    flags = (PARTIAL_MERGE if merge else 0) | (PARTIAL_FINAL if final else 0)
+    st = load().packed_kv_attention_partial(_ptr(q), n_q, arr, len(stores), C, stores[0].group, sm_scale, flags,
+                                            _ptr(o_acc), _ptr(lse_acc), int(out_fp32), _ptr(out) if final else None,
+                                            _stream(stream))
+    _check(st, "packed_kv_attention_partial")
+    return out if final else state
 
 
 def device_status(stream=None) -> int:

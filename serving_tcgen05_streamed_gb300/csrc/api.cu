@@ -286,6 +286,34 @@ int packed_kv_attention_causal(const void *q, int64_t n_q, int64_t q_pos0, const
     return attention_common(q, n_q, &r, 1, hidden, group, sm_scale, out_fp32, out, stream, 1, q_pos0);
 }
 
+int packed_kv_attention_partial(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges, int hidden,
+                                int group, float sm_scale, int flags, float *o_acc, float *lse_acc, int out_fp32,
+                                void *out, kvq_stream_t stream) {
+    if (flags < 0 || flags > (KVQ_PARTIAL_MERGE | KVQ_PARTIAL_FINAL)) return KVQ_ERR_ARG;
+    const bool merge = flags & KVQ_PARTIAL_MERGE, final = flags & KVQ_PARTIAL_FINAL;
+    if (!q || (final && !out)) return KVQ_ERR_ARG;
+    if (merge || !final) {  // the state is read (merge) or written (not final)
+        if (!o_acc || !lse_acc) return KVQ_ERR_ARG;
+        const void *st[2] = {o_acc, lse_acc};
+        for (const void *a : st)
+            if (a == q || (final && a == out)) return KVQ_ERR_ARG;
+        if (!aligned16(o_acc) || !aligned16(lse_acc)) return KVQ_ERR_ALIGN;
+    }
+    if (n_q < 1 || n_q > (int64_t(1) << 31) - 256 || !valid_hidden(hidden) || !valid_group(group)) return KVQ_ERR_ARG;
+    if (out_fp32 != 0 && out_fp32 != 1) return KVQ_ERR_ARG;
+    if (final && out_fp32 && out == q) return KVQ_ERR_ARG;
+    if (!aligned16(q) || (final && !aligned16(out))) return KVQ_ERR_ALIGN;
+    int64_t n_kv = 0;
+    if (ranges && n_ranges >= 1 && n_ranges <= KVQ_MAX_RANGES)
+        for (int i = 0; i < n_ranges; ++i) n_kv += ranges[i].len;
+    RangeTable t;
+    const int st = check_range_table(ranges, n_ranges, n_kv, hidden, group, true, &t);
+    if (st) return st;
+    if (!(sm_scale > 0.0f)) sm_scale = 0.08838834764831845f;
+    return launch_attention(q, n_q, t, hidden, group, sm_scale, out_fp32, final ? out : nullptr,
+                            reinterpret_cast<cudaStream_t>(stream), 0, 0, flags, o_acc, lse_acc);
+}
+
 int kvq_device_status(kvq_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
     unsigned int a = 0, b = 0, c = 0;

@@ -114,7 +114,14 @@ struct AttnParams {
     int tiles_before[KVQ_MAX_RANGES + 1];
     int causal;      // 1: query row i (at key position q_pos0 + i) sees keys j <= q_pos0 + i
     int64_t q_pos0;  // single store only
+    // Attention over one key chunk with a carried state (vram_lab.py's blockwise
+    // attention and `_online_combine`): 0 for the one-call attention; otherwise
+    // KVQ_PARTIAL_MERGE / KVQ_PARTIAL_FINAL bits, plus kPartial.
+    int partial;
+    float *o_acc;    // [n_q][hidden] fp32: normalised output so far, rotated basis
+    float *lse_acc;  // [n_q][heads] fp32: log sum exp(s) over the keys so far
 };
+constexpr int kPartial = 4;  // set in AttnParams::partial for every key-chunk call
 
 // Staging buffers of packed codes, filled by bulk copies: three 16 KB stages.
 // An INT4 tile takes one stage: the CTA's 64 K rows (4 KB) at offset 0 and
@@ -222,6 +229,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -842,40 +854,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         // epilogue: O / l, un-rotate, store
         if (ok && T > 0 && __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (T - 1) & 1, abort_flag, &g_err_attn))) {
             tc_fence_after();
-            uint32_t oraw[128];
-            tmem_ld128(oa, oraw);
-            const float inv_l = 1.0f / l;
-            // V^'s dims, hence O's columns, are in the order e0 e4 e1 e5 e2 e6 e3 e7 per 8-dim chunk
-            float o[128];
-#pragma unroll
-            for (int c = 0; c < 128; c += 8) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    o[c + e] = __uint_as_float(oraw[c + 2 * e]) * inv_l;
-                    o[c + 4 + e] = __uint_as_float(oraw[c + 2 * e + 1]) * inv_l;
-                }
-            }
-            rotate128_thread(o);
             const int64_t row = cta_row0<CAUSAL>() + t * BQT + r;
-            if (row < p.n_q) {
-                if (p.out_fp32) {
-                    float4 *dst =
-                        reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * p.hidden + head * 128);
+            const float inv_l = 1.0f / l;
+            // Key-chunk calls that carry a state: this chunk's o = O / l and its
+            // log-sum-exp ln sum_j e^(s_j tau) = (m + log2 l) ln 2 (the weights are
+            // 2^(s_j tau log2 e - m)), merged into the state as `_online_combine`
+            // does: new = ln(e^lse_acc + e^lse), o = o_acc e^(lse_acc - new) + o e^(lse - new).
+            // O leaves TMEM 32 columns at a time straight into the state, so no more
+            // than 32 columns are live during the merge.  A final call then reads
+            // the merged row back for the un-rotation.  The weights use the hardware
+            // exp2 / log2 approximations (relative error about 1e-7).
+            const int partial = CAUSAL ? 0 : p.partial;  // key-chunk calls are never causal
+            const bool merge = partial & KVQ_PARTIAL_MERGE, final = partial & KVQ_PARTIAL_FINAL;
+            const bool via_state = partial && (merge || !final);
+            if (via_state) {
+                constexpr float kLn2 = 0.69314718055994531f, kLog2e = 1.4426950408889634f;
+                const bool live = row < p.n_q;
+                float *acc = p.o_acc + (live ? row : 0) * p.hidden + head * 128;
+                float *lacc = p.lse_acc + (live ? row : 0) * (p.hidden >> 7) + head;
+                const float lc2 = m + lg2_approx(l);
+                float nw = lc2, wa = 0.0f, wc = inv_l;
+                if (merge && live) {
+                    const float la2 = *lacc * kLog2e;
+                    const float hi = fmaxf(la2, lc2), lo = fminf(la2, lc2);
+                    nw = hi + lg2_approx(1.0f + ex2_approx(lo - hi));
+                    wa = ex2_approx(la2 - nw);
+                    wc = ex2_approx(lc2 - nw) * inv_l;
+                }
+#pragma unroll 1
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t oc[32];
+                    tmem_ld32(oa + c0, oc);  // warp-wide: every lane loads, live or not
+                    tmem_ld_wait();
+                    if (live) {
+                        float4 *dst = reinterpret_cast<float4 *>(acc + c0);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                } else {
-                    uint4 *dst =
-                        reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + row * p.hidden + head * 128);
+                        for (int c = 0; c < 32; c += 8) {  // columns e0 e4 e1 e5 e2 e6 e3 e7 -> dims e0..e7
+                            float v[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * i + 2 * k], o[8 * i + 2 * k + 1]);
-                            w4[k] = *reinterpret_cast<const uint32_t *>(&b2);
+                            for (int e = 0; e < 4; ++e) {
+                                v[e] = __uint_as_float(oc[c + 2 * e]) * wc;
+                                v[4 + e] = __uint_as_float(oc[c + 2 * e + 1]) * wc;
+                            }
+                            if (merge) {
+                                const float4 a0 = dst[c / 4], a1 = dst[c / 4 + 1];
+                                v[0] = fmaf(a0.x, wa, v[0]);
+                                v[1] = fmaf(a0.y, wa, v[1]);
+                                v[2] = fmaf(a0.z, wa, v[2]);
+                                v[3] = fmaf(a0.w, wa, v[3]);
+                                v[4] = fmaf(a1.x, wa, v[4]);
+                                v[5] = fmaf(a1.y, wa, v[5]);
+                                v[6] = fmaf(a1.z, wa, v[6]);
+                                v[7] = fmaf(a1.w, wa, v[7]);
+                            }
+                            dst[c / 4] = make_float4(v[0], v[1], v[2], v[3]);
+                            dst[c / 4 + 1] = make_float4(v[4], v[5], v[6], v[7]);
                         }
-                        dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+                if (live && !final) *lacc = nw * kLn2;
+            }
+            if (!via_state || final) {
+                float o[128];
+                if (via_state) {  // the merged row, back from the state (this thread's own writes)
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.o_acc + (row < p.n_q ? row : 0) * p.hidden + head * 128);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float4 a = row < p.n_q ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        o[4 * i] = a.x;
+                        o[4 * i + 1] = a.y;
+                        o[4 * i + 2] = a.z;
+                        o[4 * i + 3] = a.w;
+                    }
+                } else {
+                    uint32_t oraw[128];
+                    tmem_ld128(oa, oraw);
+                    // V^'s dims, hence O's columns, are in the order e0 e4 e1 e5 e2 e6 e3 e7 per 8-dim chunk
+#pragma unroll
+                    for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            o[c + e] = __uint_as_float(oraw[c + 2 * e]) * inv_l;
+                            o[c + 4 + e] = __uint_as_float(oraw[c + 2 * e + 1]) * inv_l;
+                        }
+                    }
+                }
+                rotate128_thread(o);
+                if (row < p.n_q) {
+                    if (p.out_fp32) {
+                        float4 *dst =
+                            reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * p.hidden + head * 128);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    } else {
+                        uint4 *dst =
+                            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + row * p.hidden + head * 128);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * i + 2 * k], o[8 * i + 2 * k + 1]);
+                                w4[k] = *reinterpret_cast<const uint32_t *>(&b2);
+                            }
+                            dst[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
                     }
                 }
             }
@@ -911,7 +996,8 @@ int launch_group(const CUtensorMap &tm, const AttnParams &p, dim3 grid, bool mix
 }  // namespace
 
 int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int hidden, int group, float sm_scale,
-                     int out_fp32, void *out, cudaStream_t s, int causal, int64_t q_pos0) {
+                     int out_fp32, void *out, cudaStream_t s, int causal, int64_t q_pos0, int partial_flags,
+                     float *o_acc, float *lse_acc) {
     alignas(64) CUtensorMap tm_q;
     if (encode_tmap_2d(&tm_q, q, 1, static_cast<uint64_t>(hidden), static_cast<uint64_t>(n_q),
                        static_cast<uint64_t>(hidden) * 2, 64, BQT))
@@ -934,6 +1020,9 @@ int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int h
     p.total_tiles = tiles;
     p.causal = causal;
     p.q_pos0 = q_pos0;
+    p.partial = partial_flags < 0 ? 0 : (partial_flags | kPartial);
+    p.o_acc = o_acc;
+    p.lse_acc = lse_acc;
     // CTA pairs: an even number of CTAs of BQ query rows each
     const int64_t pairs = (n_q + 2 * BQ - 1) / (2 * BQ);
     dim3 grid(static_cast<unsigned>(2 * pairs), static_cast<unsigned>(hidden / 128));

@@ -33,8 +33,11 @@ cudaError_t launch_kv_unpack(const void *k_codes, const void *v_codes, const voi
 int launch_qkv_proj(const void *x, const void *w, int64_t n, int hidden, int group, int64_t chunk_tokens,
                     const float *q_norm_w, const float *k_norm_w, float eps, void *q_out, const RangeTable &ranges,
                     cudaStream_t s, const float *rope_cs = nullptr, int rot_dim = 0, int sections = 3);
+// partial_flags < 0: the one-call attention; otherwise a key-chunk call with
+// KVQ_PARTIAL_* flags and the carried state (o_acc, lse_acc).
 int launch_attention(const void *q, int64_t n_q, const RangeTable &ranges, int hidden, int group, float sm_scale,
-                     int out_fp32, void *out, cudaStream_t s, int causal = 0, int64_t q_pos0 = 0);
+                     int out_fp32, void *out, cudaStream_t s, int causal = 0, int64_t q_pos0 = 0,
+                     int partial_flags = -1, float *o_acc = nullptr, float *lse_acc = nullptr);
 cudaError_t launch_selftest_wait(uint64_t ns, cudaStream_t s);
 
 // Device error words, one per translation unit: read-and-clear (synchronous).

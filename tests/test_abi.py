@@ -136,6 +136,21 @@ def test_argument_errors_are_reported_before_any_launch():
     assert lib.streamed_qkv_proj_mixed(a16, a16, 10, 1024, 32, 0, None, None, 1e-6, P(2 << 20), gap_proj, 2, S) \
         == kvq.KVQ_ERR_ARG
     assert lib.kvq_selftest_wait_timeout(0, S) == kvq.KVQ_ERR_ARG
+    # attention over a key chunk with a carried state
+    ok1 = (R * 1)(R(0, 100, 128, 4, 0, 1 << 20, 1 << 20, 1 << 20, 1 << 20))
+    acc, lse, out = P(4 << 20), P(6 << 20), P(8 << 20)
+    part = lib.packed_kv_attention_partial
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 4, acc, lse, 0, out, S) == kvq.KVQ_ERR_ARG  # flags
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, -1, acc, lse, 0, out, S) == kvq.KVQ_ERR_ARG
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 0, None, lse, 0, None, S) == kvq.KVQ_ERR_ARG  # no state to start
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 1, acc, None, 0, None, S) == kvq.KVQ_ERR_ARG  # no state to merge
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 3, acc, lse, 0, None, S) == kvq.KVQ_ERR_ARG  # final, no out
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 0, a16, lse, 0, None, S) == kvq.KVQ_ERR_ARG  # state aliases q
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 3, acc, lse, 0, acc, S) == kvq.KVQ_ERR_ARG  # state aliases out
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 3, acc, lse, 1, a16, S) == kvq.KVQ_ERR_ARG  # fp32 over q
+    assert part(a16, 10, ok1, 1, 1024, 32, 0.0, 0, P((4 << 20) + 4), lse, 0, None, S) == kvq.KVQ_ERR_ALIGN
+    assert part(a16, 10, bad_gap, 2, 1024, 32, 0.0, 0, acc, lse, 0, None, S) == kvq.KVQ_ERR_ARG
+    assert part(a16, 0, ok1, 1, 1024, 32, 0.0, 0, acc, lse, 0, None, S) == kvq.KVQ_ERR_ARG
 
 
 def test_python_binding_refuses_cpu_tensors():

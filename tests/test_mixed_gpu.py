@@ -8,7 +8,9 @@ import torch
 import oracle
 import serving_tcgen05_streamed_gb300 as kvq
 from serving_tcgen05_streamed_gb300 import inputs
-from tests._util import bf16_ulp, bits16, codes_as_int, to_token_major
+from tests._fused_tol import check_q, head_bounds
+from tests._util import bits16
+from tests.test_qkv_proj_gpu import _compare
 
 pytestmark = pytest.mark.gpu
 
@@ -37,13 +39,7 @@ def test_mixed_projection_writes_each_range_at_its_precision():
     for (n, bits), st in zip(segs, stores):
         rows = np.arange(start, start + n)
         ref = oracle.qkv_proj(bits16(x), bits16(w), rows, bits=bits)
-        for cname, sname in (("k_codes", "k_scales"), ("v_codes", "v_scales")):
-            gc = to_token_major(getattr(st, cname), np.arange(n))
-            gs = to_token_major(getattr(st, sname), np.arange(n)).view(np.uint16)
-            d = np.abs(codes_as_int(gc, bits).astype(np.int32) - codes_as_int(ref[cname], bits))
-            assert d.max() <= 1 and np.mean(d != 0) <= 1e-3, (bits, cname)
-            ds = np.abs(gs.astype(np.int32) - ref[sname].astype(np.int32))
-            assert ds.max() <= 1 and np.mean(ds != 0) <= 2e-2
+        _compare(None, st, ref, np.arange(n), x[start:start + n], w, bits=bits, what=f"range of {n} at INT{bits}")
         start += n
 
 
@@ -98,19 +94,12 @@ def test_mixed_block_full_size_sampled_rows():
         picks.append(rows)
         ref = oracle.qkv_proj(bits16(x[torch.as_tensor(rows, device="cuda")]), wb, bits=bits, q_norm_w=qn_np,
                               k_norm_w=kn_np, eps=1e-6)
+        xs = x[torch.as_tensor(rows, device="cuda")]
+        c = _compare(None, st, ref, local, xs, w, qn, kn, bits=bits, what=name)
+        b = head_bounds(bits16(xs), wb, qn_np, kn_np)
         got_q = bits16(q[torch.as_tensor(rows, device="cuda")]).view(np.uint16)
-        qf = (got_q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-        rf = ref["q_f32"].astype(np.float64)
-        rms = np.sqrt(np.mean(rf.reshape(rf.shape[0], -1, 128) ** 2, axis=-1, keepdims=True))
-        floor = np.broadcast_to(1e-4 * rms, rms.shape[:2] + (128,)).reshape(rf.shape)
-        assert np.all(np.abs(qf - rf) <= bf16_ulp(rf) * 1.0001 + floor), name
-        for cname, sname in (("k_codes", "k_scales"), ("v_codes", "v_scales")):
-            gc = to_token_major(getattr(st, cname), local)
-            gs = to_token_major(getattr(st, sname), local).view(np.uint16)
-            d = np.abs(codes_as_int(gc, bits).astype(np.int32) - codes_as_int(ref[cname], bits))
-            assert d.max() <= 1 and np.mean(d != 0) <= 1e-3, (name, cname)
-            ds = np.abs(gs.astype(np.int32) - ref[sname].astype(np.int32))
-            assert ds.max() <= 1 and np.mean(ds != 0) <= 2e-2, (name, sname)
+        c.update(check_q(got_q, ref["q_f32"], ref["q_bf16"], b["q"], f"{name} q"))
+        print(name, c)
         start += sn
     # attention: the sampled query rows against every key of the four stores
     rows = np.concatenate(picks)

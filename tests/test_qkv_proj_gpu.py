@@ -1,19 +1,14 @@
 """Parity of the streamed fused QKV projection (tcgen05 GEMM + rotate /
 quantise epilogue) with the CPU oracle.
 
-Tolerances: the GEMM accumulates in a different order from the oracle, so
- - Q (BF16) must lie within one BF16 ulp of the oracle's fp32 value, plus an
-   absolute floor of 1e-4 x the RMS of that head's row for values near zero
-   (a different fp32 summation order over K <= 7168 terms moves the
-   accumulator by about sqrt(K) * 2^-24 of the terms' size, 20x below it);
- - K / V codes may differ by at most 1, on at most 0.1% of the elements;
- - scales must be equal except for at most 2% of the groups, which may
-   differ by one fp16 ulp (a relative accumulator difference d moves
-   fp16(amax/7) across a rounding boundary with probability about
-   2 * d * 2^11; with K = 7168 terms, x20 outlier channels and RMSNorm, d
-   reaches about 5e-6, i.e. about 2%).
-With inputs whose products and sums are exact (one-hot rows), everything is
-bit-exact."""
+The GEMM accumulates in a different order from the oracle, so results may
+differ where the accumulator's error moves a value across a rounding
+boundary; tests/_fused_tol.py bounds that error per head vector (the fp32
+tensor-core accumulation, then the RMSNorm, RoPE and rotation) and accepts
+a differing scale, code or Q value only where the oracle's value lies within
+the bound of the boundary it crossed.  The counts of differing values are
+printed.  With inputs whose products and sums are exact (one-hot rows),
+everything is bit-exact."""
 import numpy as np
 import pytest
 import torch
@@ -21,36 +16,38 @@ import torch
 import oracle
 import serving_tcgen05_streamed_gb300 as kvq
 from serving_tcgen05_streamed_gb300 import inputs
-from tests._util import bf16_ulp, bits16, codes_as_int, to_token_major
+from tests._fused_tol import check_kv, check_q, head_bounds
+from tests._util import bits16, to_token_major
 
 pytestmark = pytest.mark.gpu
 
 
-def _compare(q_gpu, store, ref, rows, bits=4, exact=False):
-    q = bits16(q_gpu[torch.as_tensor(rows, device=q_gpu.device)]).view(np.uint16)
-    qf = (q.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+def _compare(q_gpu, store, ref, rows, x_rows, w, qn=None, kn=None, rot_dim=0, bits=4, group=32, exact=False,
+             what=""):
+    """Checks the GPU's Q rows `rows` (None: no Q) and store rows against the
+    oracle's results `ref` for the same token rows; x_rows: those rows of x."""
+    counts = {}
     if exact:
-        assert np.array_equal(q, ref["q_bf16"])
-    else:
-        err = np.abs(qf - ref["q_f32"])
-        rf = ref["q_f32"].astype(np.float64)
-        rms = np.sqrt(np.mean(rf.reshape(rf.shape[0], -1, 128) ** 2, axis=-1, keepdims=True))
-        floor = np.broadcast_to(1e-4 * rms, rms.shape[:2] + (128,)).reshape(rf.shape)
-        assert np.all(err <= bf16_ulp(rf) * 1.0001 + floor), float((err / bf16_ulp(rf)).max())
-    for cname, sname in (("k_codes", "k_scales"), ("v_codes", "v_scales")):
-        gc = to_token_major(getattr(store, cname), rows)
-        gs = to_token_major(getattr(store, sname), rows).view(np.uint16)
-        if exact:
-            assert np.array_equal(gc, ref[cname]), cname
-            assert np.array_equal(gs, ref[sname]), sname
-            continue
-        a, b = codes_as_int(gc, bits), codes_as_int(ref[cname], bits)
-        d = np.abs(a.astype(np.int32) - b)
-        assert d.max() <= 1, cname
-        assert np.mean(d != 0) <= 1e-3, (cname, float(np.mean(d != 0)))
-        ds = np.abs(gs.astype(np.int32) - ref[sname].astype(np.int32))
-        assert ds.max() <= 1, sname
-        assert np.mean(ds != 0) <= 2e-2, sname
+        if q_gpu is not None:
+            q = bits16(q_gpu[torch.as_tensor(rows, device=q_gpu.device)]).view(np.uint16)
+            assert np.array_equal(q, ref["q_bf16"])
+        for name in ("k_codes", "v_codes", "k_scales", "v_scales"):
+            got = to_token_major(getattr(store, name), rows)
+            assert np.array_equal(got.view(np.uint16) if "scales" in name else got, ref[name]), name
+        return counts
+    tonp = lambda t: None if t is None else (t.cpu().numpy() if torch.is_tensor(t) else np.asarray(t))  # noqa: E731
+    b = head_bounds(bits16(x_rows), bits16(w), tonp(qn), tonp(kn), rot_dim=rot_dim)
+    if q_gpu is not None:
+        q = bits16(q_gpu[torch.as_tensor(rows, device=q_gpu.device)]).view(np.uint16)
+        counts.update(check_q(q, ref["q_f32"], ref["q_bf16"], b["q"], what + " q"))
+    for n in ("k", "v"):
+        gc = to_token_major(getattr(store, f"{n}_codes"), rows)
+        gs = to_token_major(getattr(store, f"{n}_scales"), rows).view(np.uint16)
+        c = check_kv(gc, gs, ref[f"{n}_codes"], ref[f"{n}_scales"], ref[f"{n}_rot"], b[n], bits, group,
+                     f"{what} {n}")
+        counts.update({f"{n}_{k}": v for k, v in c.items()})
+    print(f"{what}: {counts}")
+    return counts
 
 
 def _run(x, w, qn=None, kn=None, group=32, chunk=0):
@@ -66,7 +63,7 @@ def test_tiny_block_full():
     x, w, _, _ = inputs.block_inputs(inputs.TINY)
     q, store = _run(x, w)
     ref = oracle.qkv_proj(bits16(x), bits16(w))
-    _compare(q, store, ref, np.arange(x.shape[0]))
+    _compare(q, store, ref, np.arange(x.shape[0]), x, w, what="tiny block")
     for t in (store.k_codes, store.v_codes):
         assert int(t[:, x.shape[0]:].count_nonzero()) == 0
 
@@ -86,7 +83,7 @@ def test_one_hot_rows_are_bit_exact(group):
     w = (torch.randn((3 * C, C), generator=g) * 0.1).to(torch.bfloat16)
     q, store = _run(x, w, group=group)
     ref = oracle.qkv_proj(bits16(x), bits16(w), group=group)
-    _compare(q, store, ref, np.arange(n), exact=True)
+    _compare(q, store, ref, np.arange(n), x, w, exact=True)
 
 
 @pytest.mark.parametrize("n,C", [(1, 256), (129, 384), (1000, 1024)])
@@ -96,7 +93,7 @@ def test_ragged_sizes_and_odd_head_counts(n, C):
     w = (torch.randn((3 * C, C), generator=g) * C ** -0.5).to(torch.bfloat16)
     q, store = _run(x, w)
     ref = oracle.qkv_proj(bits16(x), bits16(w))
-    _compare(q, store, ref, np.arange(n))
+    _compare(q, store, ref, np.arange(n), x, w, what=f"n={n} C={C}")
 
 
 def test_results_do_not_depend_on_chunk_size():
@@ -141,7 +138,7 @@ def test_h3_block_with_rmsnorm_sampled_rows():
     q, store = _run(x, w, qn, kn, chunk=wl.chunk_tokens)
     rows = inputs.sample_rows(wl.n, 40, seed=4).numpy()
     ref = oracle.qkv_proj(bits16(x), bits16(w), rows, q_norm_w=qn.numpy(), k_norm_w=kn.numpy(), eps=1e-6)
-    _compare(q, store, ref, rows)
+    _compare(q, store, ref, rows, x[torch.as_tensor(rows)], w, qn, kn, what="H3 mid")
 
 
 @pytest.mark.slow
@@ -155,6 +152,6 @@ def test_h3_ref2va_full_size_sampled_rows():
     rows = inputs.sample_rows(wl.n, 24, seed=5).numpy()
     xs = x[torch.as_tensor(rows, device="cuda")]  # rows are independent: the oracle sees only the samples
     ref = oracle.qkv_proj(bits16(xs), bits16(w), q_norm_w=qn.cpu().numpy(), k_norm_w=kn.cpu().numpy())
-    _compare(q, store, ref, rows)
+    _compare(q, store, ref, rows, xs, w, qn, kn, what="H3 Ref2VA")
     # pad rows of the last tile are zero
     assert int(store.k_codes[:, wl.n:].count_nonzero()) == 0
