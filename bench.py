@@ -11,6 +11,16 @@ Prints one JSON line (rank 0).  `value` is block TFLOP/s:
 independent block (its own seed): the work per GPU is fixed (weak scaling)
 and no data crosses ranks; only the timings are reduced (max).
 
+Besides the device-timed block the line carries: the same block end to end
+through the public calls with x coming from and the output going to pinned
+host memory (e2e), the two-phase form that never holds Q or the output whole
+on the device (e2e_two_phase), the two-phase form with the packed K/V store
+itself in host memory, streamed back chunk by chunk into a key-chunked
+attention (e2e_host_staged), the standalone rotate + quantise + pack kernel
+and its inverse on K/V [262,144, 2 x 7168] (kernels.pack), the peak memory
+against materialising the BF16 QKV, and the CPU oracle's time on a sample
+(cpu_baseline).
+
 --impl reference times the CPU oracle (the plain C reference implementation
 of the same computation) on a bounded sample of the same workload.
 """
@@ -34,6 +44,9 @@ import torch  # noqa: E402
 
 E2E_IN_CHUNK = 16384   # tokens per host-to-device chunk of x in the end-to-end step
 E2E_OUT_CHUNK = 19456  # query rows per attention launch in the end-to-end step (38 CTA pairs)
+E2E_KV_CHUNK = 16384   # keys per host-staged chunk of the packed store
+E2E_STEPS, E2E_WARMUP = 10, 2  # end-to-end steps timed (at most --steps), after these untimed ones
+PACK_N = 262144        # the standalone pack / unpack record: K/V [N, 2 x 7168], group 32
 METRIC = "block TFLOP/s + tokens/s (QKV GEMM + INT4-KV attn) at N=152,263; peak GiB"
 GiB = 2.0 ** 30
 
@@ -175,12 +188,31 @@ def job_value(world: int, rank_ms_total: float, steps: int, flops_per_block: flo
 
 
 # --------------------------------------------------------------------------- CPU oracle (reference arm / baseline)
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 class CpuOracleSample:
     """The CPU oracle on a bounded sample of the block: the projection of
-    `proj_rows` token rows and the attention of `attn_rows` query rows (all
-    heads, all N keys).  Both are exact per row, so time per row extrapolates
-    to the whole block.  Inputs come from the seeded generators (generated
-    once, on the GPU when there is one, and copied to the host)."""
+    token rows and the attention of query rows (all heads, all N keys).  Both
+    are exact per row, so the time per row extrapolates to the whole block.
+    Inputs come from the seeded generators (generated once, on the GPU when
+    there is one, and copied to the host)."""
 
     def __init__(self, wl, seed: int, proj_rows: int, attn_rows: int):
         import oracle
@@ -205,20 +237,31 @@ class CpuOracleSample:
         self.q = as_u16(inputs.random_q(attn_rows, C, seed=seed))
         oracle.build()
         self.cores = oracle.threads()
-        self.sample = (f"{proj_rows} projection rows + {attn_rows} attention query rows ({heads} heads x {n} keys); "
-                       f"time per row extrapolated to N={n}")
 
-    def run(self):
-        """Returns extrapolated block seconds."""
+    def describe(self, proj_rows: int, attn_rows: int) -> str:
+        return (f"{proj_rows} projection rows + {attn_rows} attention query rows ({self.wl.heads} heads x "
+                f"{self.wl.n} keys); time per row extrapolated to N={self.wl.n}")
+
+    def time_rows(self, proj_rows: int, attn_rows: int, threads: int | None = None):
+        """Seconds per projection row and per attention query row, on `threads`
+        OpenMP threads (default: all)."""
         import oracle
-        n = self.wl.n
-        t0 = time.perf_counter()
-        oracle.qkv_proj(self.xb, self.wb, q_norm_w=self.qn, k_norm_w=self.kn)
-        t_proj = (time.perf_counter() - t0) / self.xb.shape[0]
-        t0 = time.perf_counter()
-        oracle.attention(self.q, self.kc, self.vc, self.ks, self.vs, n_kv=n)
-        t_attn = (time.perf_counter() - t0) / self.q.shape[0]
-        return t_proj * n + t_attn * n
+        oracle.set_threads(threads or self.cores)
+        try:
+            t0 = time.perf_counter()
+            oracle.qkv_proj(self.xb[:proj_rows], self.wb, q_norm_w=self.qn, k_norm_w=self.kn)
+            t_proj = (time.perf_counter() - t0) / proj_rows
+            t0 = time.perf_counter()
+            oracle.attention(self.q[:attn_rows], self.kc, self.vc, self.ks, self.vs, n_kv=self.wl.n)
+            t_attn = (time.perf_counter() - t0) / attn_rows
+        finally:
+            oracle.set_threads(self.cores)
+        return t_proj, t_attn
+
+    def run(self, proj_rows: int, attn_rows: int, threads: int | None = None) -> float:
+        """Extrapolated block seconds."""
+        t_proj, t_attn = self.time_rows(proj_rows, attn_rows, threads)
+        return (t_proj + t_attn) * self.wl.n
 
 
 def run_reference(args, wl, world, rank):
@@ -227,7 +270,7 @@ def run_reference(args, wl, world, rank):
     cpu = CpuOracleSample(wl, seed=100, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
     secs = []
     for i in range(args.warmup + args.steps):
-        t = cpu.run()
+        t = cpu.run(args.ref_proj_rows, args.ref_attn_rows)
         if i >= args.warmup:
             secs.append(t)
     t_block = sum(secs) / len(secs)
@@ -239,10 +282,32 @@ def run_reference(args, wl, world, rank):
         "config": {"workload": wl.name, "n_tokens": wl.n, "hidden": wl.hidden, "heads": wl.heads, "group": 32,
                    "kv_bits": 4},
         "tokens_per_s": wl.n / t_block,
-        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu.cores, "kind": "oracle", "sample": cpu.sample},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu.cores, "kind": "oracle",
+                         "sample": cpu.describe(args.ref_proj_rows, args.ref_attn_rows) + " (extrapolated)",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, fp: float, fa: float, proj_rows: int, attn_rows: int, single_proj_rows: int,
+                 single_attn_rows: int) -> dict:
+    """The oracle on the host cores: all cores on the CPU-baseline plan's sample
+    (projection rows + query rows, per-row times extrapolated to the block),
+    and one core on a smaller sample."""
+    n = wl.n
+    sample = CpuOracleSample(wl, seed=7, proj_rows=max(proj_rows, single_proj_rows),
+                             attn_rows=max(attn_rows, single_attn_rows))
+    tp, ta = sample.time_rows(proj_rows, attn_rows)
+    tp1, ta1 = sample.time_rows(single_proj_rows, single_attn_rows, threads=1)
+    return {"value": (fp + fa) / ((tp + ta) * n) / 1e12, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
+            "sample": sample.describe(proj_rows, attn_rows) + " (extrapolated)",
+            "cpu_model": cpu_model(),
+            "s_per_projection_row": tp, "s_per_query_row": ta, "block_s_extrapolated": (tp + ta) * n,
+            "single_core": {"value": (fp + fa) / ((tp1 + ta1) * n) / 1e12, "unit": "TFLOP/s", "cores": 1,
+                            "sample": sample.describe(single_proj_rows, single_attn_rows) + " (extrapolated)",
+                            "s_per_projection_row": tp1, "s_per_query_row": ta1,
+                            "block_s_extrapolated": (tp1 + ta1) * n}}
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -346,12 +411,13 @@ def run_gpu(args, wl, world, rank, local):
         attend_rows(q, 0)
 
     def step():
+        ev_p0.record(stream)
         project(x)
         ev_a0.record(stream)
         attend()
         ev_a1.record(stream)
 
-    ev_a0, ev_a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_p0, ev_a0, ev_a1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -364,13 +430,14 @@ def run_gpu(args, wl, world, rank, local):
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    attn_ms = []
+    attn_ms, proj_ms = [], []
     for i in range(args.steps):
         starts[i].record(stream)
         step()
         ends[i].record(stream)
         ends[i].synchronize()
         attn_ms.append(ev_a0.elapsed_time(ev_a1))
+        proj_ms.append(ev_p0.elapsed_time(ev_a0))
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
@@ -430,9 +497,9 @@ def run_gpu(args, wl, world, rank, local):
                 out_host[s0:s0 + ln].copy_(qc, non_blocking=True)
         torch.cuda.synchronize()
 
-    e2e_steps = max(1, min(args.steps, 3))
-    for i in range(1 + e2e_steps):
-        if i == 1:
+    e2e_steps = max(1, min(args.steps, E2E_STEPS))
+    for i in range(E2E_WARMUP + e2e_steps):
+        if i == E2E_WARMUP:
             torch.cuda.synchronize()
             barrier(world)
             t0 = time.perf_counter()
@@ -495,8 +562,8 @@ def run_gpu(args, wl, world, rank, local):
             ev["out"][b].record(copy)
         torch.cuda.synchronize()
 
-    for i in range(1 + e2e_steps):
-        if i == 1:
+    for i in range(E2E_WARMUP + e2e_steps):
+        if i == E2E_WARMUP:
             torch.cuda.synchronize()
             barrier(world)
             t0 = time.perf_counter()
@@ -507,9 +574,31 @@ def run_gpu(args, wl, world, rank, local):
     resident_gib = (sum(st_.nbytes() for st_ in stores) + (fine.nbytes() if route else 0)) / GiB
     assert kvq.device_status() == kvq.KVQ_OK
 
+    # ------------------------------------------------------------ end to end, packed store staged in host memory
+    # vram_lab.py's streamed block plans K/V kept in host memory and streamed to the
+    # device block by block.  Phase 1 projects K/V only, by token chunks of x from
+    # the host, into a device chunk store whose rows go to pinned host memory, one
+    # contiguous buffer per key chunk.  Phase 2 brings x in again by query chunks,
+    # recomputes their Q and attends the host-staged store key chunk by key chunk
+    # (copied in on the copy stream, two device buffers), merging each chunk into a
+    # carried log-sum-exp state; the last chunk writes the output over Q, which goes
+    # back to the host.  The device holds W, chunk buffers and the state only: the
+    # footprint does not grow with N.
+    hs = None
+    if not args.no_host_staged and not mixed and not causal and rope is None:
+        hs = host_staged_leg(kvq, wl, w, qn, kn, x_host, out_host, stream, copy, dev, world, e2e_steps,
+                             out_chunks)
+        hs["value"] = world * (fp + fa) / hs.pop("seconds") / 1e12
+        assert kvq.device_status() == kvq.KVQ_OK
+
+    pack = None
+    if not args.no_pack_record and rank == 0:
+        pack = pack_record(kvq, dev, warmup=3, steps=10)
+
     # ------------------------------------------------------------ roofline of the dominant kernel (attention)
     peaks, peak_kind = load_peaks()
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    proj_avg_ms = sum(proj_ms) / len(proj_ms)
     attn_tflops = fa / (attn_avg_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     traffic = None  # DRAM bytes per launch from an ncu capture of the same attention code, else null
@@ -523,10 +612,8 @@ def run_gpu(args, wl, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not mixed and not causal and rope is None:
         del x_host, out_host
-        sample = CpuOracleSample(wl, seed=7, proj_rows=args.ref_proj_rows, attn_rows=args.ref_attn_rows)
-        t_block = sample.run()
-        cpu = {"value": (fp + fa) / t_block / 1e12, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
-               "sample": sample.sample}
+        cpu = cpu_baseline(wl, fp, fa, args.cpu_proj_rows, args.cpu_attn_rows, args.cpu_single_proj_rows,
+                           args.cpu_single_attn_rows)
 
     if rank == 0:
         line = {
@@ -543,9 +630,8 @@ def run_gpu(args, wl, world, rank, local):
                              f"{sum(st.nbytes() for st in stores) / GiB:.2f} GiB)",
                        "parallelism": f"independent blocks x{world}"},
             "tokens_per_s": world * n / (ms_per_step * 1e-3),
-            "kernel_ms": {"qkv_proj": ms_per_step - attn_avg_ms, "attention": attn_avg_ms},
-            "kernel_tflops": {"qkv_proj": fp / ((ms_per_step - attn_avg_ms) * 1e-3) / 1e12,
-                              "attention": attn_tflops},
+            "kernel_ms": {"qkv_proj": proj_avg_ms, "attention": attn_avg_ms},
+            "kernel_tflops": {"qkv_proj": fp / (proj_avg_ms * 1e-3) / 1e12, "attention": attn_tflops},
             "peak_gib": peak_ours, "peak_gib_materialise_bf16_qkv": peak_mat,
             "peak_ratio": peak_ours / peak_mat if peak_mat else None,
             "kv_store": [{"tokens": st.n, "bits": st.bits} for st in stores],
@@ -567,11 +653,155 @@ def run_gpu(args, wl, world, rank, local):
                                       "query chunks, Q only recomputed, attention, output chunk back to the host; "
                                       "device_gib = packed store + chunk buffers (x, Q and output never held in "
                                       "full), W excluded as in the peak comparison"},
+            "e2e_host_staged": hs,
+            "kernels": {"pack": pack} if pack else None,
             # per step: the projection (and, routed, the fine store's K/V section) and the attention calls
             "gpu_launches": ((2 + len(routed_segs)) if route else 2) * args.steps,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
+
+
+def host_staged_leg(kvq, wl, w, qn, kn, x_host, out_host, stream, copy, dev, world, steps, out_chunks):
+    """The block end to end with the packed K/V store in pinned host memory (see
+    the comment at its call).  Returns seconds per step, device memory and the
+    bytes copied each way."""
+    n, C = wl.n, wl.hidden
+    heads = C // 128
+    kv_chunks = [(s0, min(E2E_KV_CHUNK, n - s0)) for s0 in range(0, n, E2E_KV_CHUNK)]
+    assert E2E_KV_CHUNK <= E2E_IN_CHUNK  # phase 1 lands x by key chunks in the x chunk buffers
+    torch.cuda.synchronize()
+    mem0 = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+
+    def host_chunk():
+        return kvq.PackedKV(
+            torch.empty((heads, E2E_KV_CHUNK, 64), dtype=torch.uint8, pin_memory=True),
+            torch.empty((heads, E2E_KV_CHUNK, 64), dtype=torch.uint8, pin_memory=True),
+            torch.empty((heads, E2E_KV_CHUNK, 4), dtype=torch.float16, pin_memory=True),
+            torch.empty((heads, E2E_KV_CHUNK, 4), dtype=torch.float16, pin_memory=True), E2E_KV_CHUNK, 4, 32)
+
+    host_kv = [host_chunk() for _ in kv_chunks]
+    kv_dev = [kvq.PackedKV.empty(E2E_KV_CHUNK, C, 32, 4, dev) for _ in range(2)]
+    xb = [torch.empty((E2E_IN_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    xq = [torch.empty((E2E_OUT_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    qb = [torch.empty((E2E_OUT_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    o_acc, lse_acc = kvq.partial_state(E2E_OUT_CHUNK, C, dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in1", "p1", "kvout", "in2", "qp", "kvin", "attn",
+                                                              "out")}
+    parts = lambda st: (st.k_codes, st.v_codes, st.k_scales, st.v_scales)  # noqa: E731
+
+    def one_step():
+        for i, (s0, ln) in enumerate(kv_chunks):  # phase 1: K/V of every token, to the host
+            b = i % 2
+            copy.wait_event(ev["p1"][b])
+            with torch.cuda.stream(copy):
+                xb[b][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+            ev["in1"][b].record(copy)
+            stream.wait_event(ev["in1"][b])
+            stream.wait_event(ev["kvout"][b])  # the chunk store of chunk i-2 has gone to the host
+            kvq.streamed_qkv_proj_ex(xb[b][:ln], w, [kv_dev[b].rows(0, ln)], sections=kvq.SECTION_KV, group=32,
+                                     chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, stream=stream)
+            ev["p1"][b].record(stream)
+            copy.wait_event(ev["p1"][b])
+            with torch.cuda.stream(copy):
+                for d, s_ in zip(parts(host_kv[i]), parts(kv_dev[b])):
+                    d.copy_(s_, non_blocking=True)
+            ev["kvout"][b].record(copy)
+        kc = 0
+        for i, (s0, ln) in enumerate(out_chunks):  # phase 2: Q per query chunk, the store streamed in
+            b = i % 2
+            if i == 0:
+                with torch.cuda.stream(copy):
+                    xq[0][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+                ev["in2"][0].record(copy)
+            stream.wait_event(ev["in2"][b])
+            stream.wait_event(ev["out"][b])
+            qc = kvq.streamed_qkv_proj_ex(xq[b][:ln], w, None, sections=kvq.SECTION_Q, group=32,
+                                          chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn,
+                                          q_out=qb[b][:ln], stream=stream)
+            ev["qp"][b].record(stream)
+            if i + 1 < len(out_chunks):  # next chunk's x, once the projection of chunk i-1 has read it
+                s1, l1 = out_chunks[i + 1]
+                copy.wait_event(ev["qp"][1 - b])
+                with torch.cuda.stream(copy):
+                    xq[1 - b][:l1].copy_(x_host[s1:s1 + l1], non_blocking=True)
+                ev["in2"][1 - b].record(copy)
+            state = (o_acc[:ln], lse_acc[:ln])
+            for j, (k0, kl) in enumerate(kv_chunks):
+                kb = kc % 2
+                kc += 1
+                copy.wait_event(ev["attn"][kb])  # the attention that last read this buffer has run
+                with torch.cuda.stream(copy):
+                    for d, s_ in zip(parts(kv_dev[kb]), parts(host_kv[j])):
+                        d.copy_(s_, non_blocking=True)
+                ev["kvin"][kb].record(copy)
+                stream.wait_event(ev["kvin"][kb])
+                last = j == len(kv_chunks) - 1
+                kvq.packed_kv_attention_partial(qc, [kv_dev[kb].rows(0, kl)], state=state, merge=j > 0, final=last,
+                                                out=qc if last else None, stream=stream)
+                ev["attn"][kb].record(stream)
+            copy.wait_event(ev["attn"][(kc - 1) % 2])
+            with torch.cuda.stream(copy):
+                out_host[s0:s0 + ln].copy_(qc, non_blocking=True)
+            ev["out"][b].record(copy)
+        torch.cuda.synchronize()
+
+    for i in range(E2E_WARMUP + steps):
+        if i == E2E_WARMUP:
+            torch.cuda.synchronize()
+            barrier(world)
+            t0 = time.perf_counter()
+        one_step()
+    secs = max_over_ranks(world, (time.perf_counter() - t0) / steps)
+    peak = (torch.cuda.max_memory_allocated(dev) - mem0) / GiB
+    store_bytes = sum(t.numel() * t.element_size() for st in host_kv for t in parts(st))
+    return {"unit": "TFLOP/s", "ms_per_step": secs * 1e3, "seconds": secs,
+            "device_gib": peak, "host_store_gib": store_bytes / GiB,
+            "h2d_bytes_per_step": int(2 * n * C * 2 + len(out_chunks) * store_bytes),
+            "d2h_bytes_per_step": int(store_bytes + n * C * 2),
+            "key_chunk": E2E_KV_CHUNK, "query_chunk": E2E_OUT_CHUNK,
+            "note": "packed K/V in pinned host memory, one buffer per key chunk of "
+                    f"{E2E_KV_CHUNK}; phase 1 projects K/V by token chunks and sends them to the host; phase 2 "
+                    "recomputes Q per query chunk and attends the store chunk by chunk (packed_kv_attention_partial, "
+                    "log-sum-exp state), each chunk copied in while the previous one is attended; device_gib = "
+                    "chunk buffers + state, W excluded"}
+
+
+def pack_record(kvq, dev, warmup: int, steps: int) -> dict:
+    """kv_rotate_quant_pack and kv_unpack on K/V [PACK_N, 2 x 7168] BF16, group
+    32, INT4: median CUDA-event time over `steps` launches, L2 flushed (a 512 MiB
+    write) before each, against the measured HBM copy bandwidth."""
+    from serving_tcgen05_streamed_gb300 import inputs
+    C, g = 7168, 32
+    peaks, kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    kv = inputs.sweep_kv(PACK_N, C, seed=0, device=dev)
+    store = kvq.PackedKV.empty(PACK_N, C, g, 4, dev)
+    out = torch.empty_like(kv)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    nbytes = PACK_N * (2 * C * 2 + 2 * (C // 2 + (C // g) * 2))  # BF16 K/V + INT4 codes + fp16 scales
+    rec = {"n": PACK_N, "hidden": C, "group": g, "bits": 4, "bytes_per_launch": nbytes, "peak_gbs": hbm,
+           "peak_source": f"{kind} hbm copy", "l2": "flushed before every launch"}
+    for name, fn in (("kv_rotate_quant_pack", lambda: kvq.kv_rotate_quant_pack(kv, C, g, 4, out=store)),
+                     ("kv_unpack", lambda: kvq.kv_unpack(store, C, out=out))):
+        ts = []
+        for i in range(warmup + steps):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            if i >= warmup:
+                ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rec[name] = {"ms": ms, "gbs": gbs, "frac": gbs / hbm}
+    assert kvq.device_status() == kvq.KVQ_OK
+    del kv, store, out, flush
+    torch.cuda.empty_cache()
+    return rec
 
 
 def run_sweep(args):
@@ -636,8 +866,22 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--ref-proj-rows", type=int, default=16)
-    ap.add_argument("--ref-attn-rows", type=int, default=16)
+    ap.add_argument("--ref-proj-rows", type=int, default=128,
+                    help="reference arm: projection rows of the oracle per step")
+    ap.add_argument("--ref-attn-rows", type=int, default=32,
+                    help="reference arm: attention query rows of the oracle per step")
+    ap.add_argument("--cpu-proj-rows", type=int, default=1024,
+                    help="cpu_baseline (all cores): projection rows")
+    ap.add_argument("--cpu-attn-rows", type=int, default=256,
+                    help="cpu_baseline (all cores): attention query rows")
+    ap.add_argument("--cpu-single-proj-rows", type=int, default=32,
+                    help="cpu_baseline (one core): projection rows")
+    ap.add_argument("--cpu-single-attn-rows", type=int, default=4,
+                    help="cpu_baseline (one core): attention query rows")
+    ap.add_argument("--no-pack-record", action="store_true",
+                    help="skip the standalone pack / unpack record")
+    ap.add_argument("--no-host-staged", action="store_true",
+                    help="skip the end-to-end leg with the packed store in host memory")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=("h3_ref2va", "mid", "mixed", "causal", "sweep"), default="h3_ref2va",
                     help="h3_ref2va: N=152,263 (the benchmark); mid: N=16,384 at the same width (profiling); "

@@ -42,6 +42,13 @@
  *    reads, and the kernel returns early (its outputs are then undefined).
  *  - Inputs must be finite, and rotated Q, K and V values must lie within the
  *    fp16 range (|v| < 65504): the attention computes on fp16 operands.
+ *  - Score range of the attention: the dequantised K^ operand is rounded to
+ *    fp16 (11 significant bits), which moves a score s = sm_scale q.k^ by
+ *    about |s| 2^-12 and an output by that much of |v|.  The parity bar
+ *    (max-abs 1e-2, relative L2 5e-3 against the exact attention on the same
+ *    packed K/V) is met for row maxima |s| up to about 35 (measured; Q and K
+ *    RMS-normalised per head reach about 14); at |s| ~ 70 the max-abs error
+ *    reaches about 1.2e-2 while the relative L2 error stays near 1e-3.
  */
 #ifndef KVQ_H
 #define KVQ_H

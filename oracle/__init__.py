@@ -83,6 +83,8 @@ def _load():
             lib.kvqo_partial_finish.argtypes = [P, I64, P]
             lib.kvqo_threads.restype = I
             lib.kvqo_threads.argtypes = []
+            lib.kvqo_set_threads.restype = None
+            lib.kvqo_set_threads.argtypes = [I]
             _lib = lib
     return _lib
 
@@ -98,6 +100,11 @@ def _c(a, dtype):
 def threads() -> int:
     """OpenMP threads the oracle runs with."""
     return int(_load().kvqo_threads())
+
+
+def set_threads(n: int) -> None:
+    """OpenMP threads for later oracle calls."""
+    _load().kvqo_set_threads(int(n))
 
 
 # ----------------------------------------------------------------- number formats

@@ -626,6 +626,11 @@ void kvqo_partial_finish(const double *o, int64_t n_vec, float *out) {
 #ifdef _OPENMP
 #include <omp.h>
 int kvqo_threads(void) { return omp_get_max_threads(); }
+/* Sets the OpenMP threads of later calls (n >= 1). */
+void kvqo_set_threads(int n) {
+    if (n >= 1) omp_set_num_threads(n);
+}
 #else
 int kvqo_threads(void) { return 1; }
+void kvqo_set_threads(int n) { (void)n; }
 #endif

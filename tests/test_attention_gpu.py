@@ -144,9 +144,10 @@ def test_h3_ref2va_full_size_sampled_rows():
 # relative, so the output error grows with the size of the scores.  Q and K
 # RMS-normalised per head (the H3 block) keep |s| <= |q||k| tau ~ 11.3 (x the
 # norm weights, ~14).  Q drawn with std sigma against the random store gives
-# scores with an RMS of about 1.3 sigma and row maxima of about 4 sigma; the
-# bar is asserted up to sigma = 8 (row maxima around 32, twice the normalised
-# range) and the errors beyond it are recorded.
+# row maxima of |s| of about 9 sigma.  Measured on a GB300: sigma 2, 4, 8, 16
+# reach max |s| 17, 35, 70, 139 with max-abs 2.8e-3, 7.5e-3, 1.15e-2, ... and
+# relative L2 about 1e-3.  The bar is asserted up to sigma = 4 (max |s| ~ 35,
+# more than twice the normalised range); beyond it the errors are recorded.
 @pytest.mark.parametrize("std", [2.0, 4.0, 8.0, 16.0, 32.0])
 def test_score_range_sweep(std):
     heads, n, nq = 2, 2000, 256
@@ -169,5 +170,5 @@ def test_score_range_sweep(std):
         k = c * np.repeat(kd[1][h, :n].view(np.float16).astype(np.float64), 32, axis=-1)
         smax = max(smax, float(np.abs(qf[:, h] @ k.T).max()) / np.sqrt(128))
     print(f"q std {std}: max |score| {smax:.1f}, max-abs {err:.3e}, rel-L2 {rel:.3e}")
-    if std <= 8.0:
+    if std <= 4.0:
         assert err <= 1e-2 and rel <= 5e-3, (err, rel)

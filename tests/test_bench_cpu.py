@@ -30,3 +30,15 @@ def test_attention_code_hash_is_stable_and_the_record_is_well_formed():
     assert re.fullmatch(r"[0-9a-f]{64}", rec["code_sha256"])
     assert rec["bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
     assert rec["workload"].startswith("H3 Ref2VA block N=152263")
+
+
+def test_cpu_baseline_record_on_the_tiny_block():
+    # all-core and one-core oracle timings, per-row times extrapolated to the block
+    from serving_tcgen05_streamed_gb300 import inputs
+    b = _bench()
+    fp, fa = b.flops(inputs.TINY.n, inputs.TINY.hidden)
+    rec = b.cpu_baseline(inputs.TINY, fp, fa, proj_rows=4, attn_rows=2, single_proj_rows=2, single_attn_rows=1)
+    assert rec["kind"] == "oracle" and rec["cores"] >= 1 and rec["single_core"]["cores"] == 1
+    assert rec["value"] > 0 and rec["single_core"]["value"] > 0
+    assert abs(rec["block_s_extrapolated"] - (rec["s_per_projection_row"] + rec["s_per_query_row"]) * 1024) < 1e-9
+    assert isinstance(rec["cpu_model"], str) and rec["cpu_model"]
