@@ -33,8 +33,11 @@
  *    a multiple of 128); rows n..cap-1 are written as zero codes and scales.
  *  - Q and attention outputs are token-major [n][hidden] with head h at
  *    columns h*128 .. h*128+127; BF16 unless stated.
- *  - All device pointers are caller-owned and must be 16-byte aligned.  The
- *    library allocates no device memory and keeps no workspace.
+ *  - All device pointers are caller-owned and must be 16-byte aligned, except
+ *    the scales pointers of a range table (kvq_range), which need only the
+ *    alignment of one scales row (2 * 128 / group bytes), so that a range may
+ *    be a window starting at any row of a store.  The library allocates no
+ *    device memory and keeps no workspace.
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream)
  *    and never synchronise.  Argument errors are reported before any launch;
  *    launch failures return KVQ_ERR_CUDA.  Every device-side wait is bounded:

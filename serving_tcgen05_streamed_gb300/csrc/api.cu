@@ -70,7 +70,7 @@ int report_cuda(cudaError_t e, const char *what) {
 namespace {
 int check_range_table(const kvq_range *ranges, int n_ranges, int64_t n, int hidden, int group, bool need_ptrs,
                       RangeTable *out) {
-    if (!ranges || n_ranges < 1 || n_ranges > KVQ_MAX_RANGES) return KVQ_ERR_ARG;
+    if (!ranges || n_ranges < 1 || n_ranges > KVQ_MAX_RANGES || !valid_group(group)) return KVQ_ERR_ARG;
     int64_t next = 0;
     std::memset(out, 0, sizeof(*out));
     out->n = n_ranges;
@@ -79,7 +79,12 @@ int check_range_table(const kvq_range *ranges, int n_ranges, int64_t n, int hidd
         if (r.start != next || r.len < 1 || r.cap < r.len || r.cap % KVQ_ROW_TILE) return KVQ_ERR_ARG;
         if (r.bits != 4 && r.bits != 8) return KVQ_ERR_ARG;
         if (need_ptrs && (!r.k_codes || !r.v_codes || !r.k_scales || !r.v_scales)) return KVQ_ERR_ARG;
-        if (!aligned16(r.k_codes) || !aligned16(r.v_codes) || !aligned16(r.k_scales) || !aligned16(r.v_scales))
+        // codes rows are 64 or 128 bytes and move by bulk copies: 16-byte aligned; scales
+        // are read and written one row (2 * 128 / group bytes) at a time, so a window
+        // starting at any row of an aligned store is aligned enough
+        const uintptr_t srow = 2u * static_cast<uintptr_t>(128 / group);
+        if (!aligned16(r.k_codes) || !aligned16(r.v_codes) || (reinterpret_cast<uintptr_t>(r.k_scales) % srow) ||
+            (reinterpret_cast<uintptr_t>(r.v_scales) % srow))
             return KVQ_ERR_ALIGN;
         next += r.len;
         RangeDev &d = out->r[i];
@@ -94,7 +99,6 @@ int check_range_table(const kvq_range *ranges, int n_ranges, int64_t n, int hidd
     }
     if (next != n) return KVQ_ERR_ARG;
     (void)hidden;
-    (void)group;
     return KVQ_OK;
 }
 

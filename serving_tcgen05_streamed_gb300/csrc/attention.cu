@@ -893,8 +893,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                             float v[8];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                v[e] = __uint_as_float(oc[c + 2 * e]) * wc;
-                                v[4 + e] = __uint_as_float(oc[c + 2 * e + 1]) * wc;
+                                v[e] = __fmul_rn(__uint_as_float(oc[c + 2 * e]), wc);
+                                v[4 + e] = __fmul_rn(__uint_as_float(oc[c + 2 * e + 1]), wc);
                             }
                             if (merge) {
                                 const float4 a0 = dst[c / 4], a1 = dst[c / 4 + 1];
@@ -930,13 +930,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 } else {
                     uint32_t oraw[128];
                     tmem_ld128(oa, oraw);
-                    // V^'s dims, hence O's columns, are in the order e0 e4 e1 e5 e2 e6 e3 e7 per 8-dim chunk
+                    // V^'s dims, hence O's columns, are in the order e0 e4 e1 e5 e2 e6 e3 e7 per 8-dim chunk.
+                    // The products are rounded on their own (never contracted into the first
+                    // butterfly), so every instantiation of the kernel gives the same bits.
 #pragma unroll
                     for (int c = 0; c < 128; c += 8) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            o[c + e] = __uint_as_float(oraw[c + 2 * e]) * inv_l;
-                            o[c + 4 + e] = __uint_as_float(oraw[c + 2 * e + 1]) * inv_l;
+                            o[c + e] = __fmul_rn(__uint_as_float(oraw[c + 2 * e]), inv_l);
+                            o[c + 4 + e] = __fmul_rn(__uint_as_float(oraw[c + 2 * e + 1]), inv_l);
                         }
                     }
                 }

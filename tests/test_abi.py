@@ -171,3 +171,19 @@ def test_store_row_window_keeps_the_head_stride():
     assert win.k_scales.data_ptr() - st.k_scales.data_ptr() == 256 * 4 * 2
     win.v_codes[1, 0, 0] = 7
     assert st.v_codes[1, 256, 0] == 7
+
+
+def test_range_scales_need_only_row_alignment():
+    # a window may start at any row: scales pointers are checked against one
+    # scales row (2 * 128 / group bytes), codes pointers against 16 bytes
+    lib = kvq.load()
+    R, P = _lib._Range, ctypes.c_void_p
+    base = 1 << 20
+    # (acceptance of row-aligned windows needs a launch: the GPU tests attend windows at odd rows)
+    for group, row in ((32, 8), (64, 4), (128, 2)):
+        bad = (R * 1)(R(0, 100, 128, 4, 0, base, base, base + row // 2, base))
+        badc = (R * 1)(R(0, 100, 128, 4, 0, base + 8, base, base, base))
+        assert lib.packed_kv_attention_partial(P(4 << 20), 10, bad, 1, 1024, group, 0.0, 0, P(6 << 20),
+                                               P(8 << 20), 0, None, None) == kvq.KVQ_ERR_ALIGN
+        assert lib.packed_kv_attention_partial(P(4 << 20), 10, badc, 1, 1024, group, 0.0, 0, P(6 << 20),
+                                               P(8 << 20), 0, None, None) == kvq.KVQ_ERR_ALIGN

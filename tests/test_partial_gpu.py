@@ -27,6 +27,8 @@ LSE_ABS = 5e-3  # score error from the FP16 K^ operand: about |s| 2^-12, a few 1
 def _store(heads, n, group=32, bits=4, seed=0, device="cuda"):
     cap = kvq.padded_rows(n)
     kc, vc, ks, vs = inputs.random_packed_kv(heads, n, cap, group, bits, seed=seed, device=device)
+    if bits == 8:  # INT8 codes are about 18x finer: keep K.q scores and V of the INT4 stores' size
+        ks, vs = (ks.float() / 18).half(), (vs.float() / 18).half()
     return kvq.PackedKV(kc.to("cuda"), vc.to("cuda"), ks.to("cuda"), vs.to("cuda"), n, bits, group)
 
 
