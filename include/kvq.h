@@ -78,7 +78,8 @@ enum kvq_status {
     KVQ_ERR_ALIGN = 2,       /* a pointer or leading dimension is not 16-byte aligned */
     KVQ_ERR_UNSUPPORTED = 3, /* a valid but unsupported combination (a RoPE width other than 64 or 128) */
     KVQ_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
-    KVQ_ERR_TIMEOUT = 5      /* a device-side wait ran out (see kvq_device_status) */
+    KVQ_ERR_TIMEOUT = 5,     /* a device-side wait ran out (see kvq_device_status) */
+    KVQ_ERR_TOO_LARGE = 6    /* the request needs more than the library's fixed state area */
 };
 
 #define KVQ_HEAD_DIM 128
@@ -263,6 +264,37 @@ KVQ_API int packed_kv_attention_mixed(const void *q, int64_t n_q, const kvq_rang
 KVQ_API int packed_kv_attention_partial(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges,
                                         int hidden, int group, float sm_scale, int flags, float *o_acc,
                                         float *lse_acc, int out_fp32, void *out, kvq_stream_t stream);
+
+/* ---------------------------------------------------------------- the key-chunk attention without caller memory
+ * This call has no counterpart on the pages; it serves callers that cannot
+ * allocate device memory.  Code that runs inside a host owning all device
+ * memory (a server's or framework's pool, a plugin with a fixed budget) and
+ * given no workspace, or on a path where cudaMalloc is not allowed because it
+ * may synchronise the device, cannot provide the o_acc / lse_acc buffers of
+ * packed_kv_attention_partial.  This variant keeps that state in a fixed area
+ * of device memory owned by the library: KVQ_STATIC_STATE_BYTES (16 MiB),
+ * reserved on every device that loads the library and held until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, flags and results are those of packed_kv_attention_partial
+ * without o_acc / lse_acc; the caller still passes Q, the key chunk (ranges)
+ * and, with KVQ_PARTIAL_FINAL, the output.  A query set of n_q rows needs
+ * n_q * (hidden + hidden / 128) * 4 bytes of state; larger requests return
+ * KVQ_ERR_TOO_LARGE (at hidden 7168: at most 580 query rows).
+ *
+ * The state area is one per device and shared by every call: a call without
+ * KVQ_PARTIAL_MERGE overwrites it (nothing needs clearing), and a later call
+ * with KVQ_PARTIAL_MERGE continues from whatever the last call left.  So one
+ * sequence of calls (start, merges, final) runs at a time per device: calls
+ * that overlap on the GPU (two sequences on different streams) race on the
+ * area.  The first call on a device looks up the area's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Errors as packed_kv_attention_partial, plus
+ * KVQ_ERR_TOO_LARGE. */
+#define KVQ_STATIC_STATE_BYTES (16u << 20)
+KVQ_API int packed_kv_attention_partial_static(const void *q, int64_t n_q, const kvq_range *ranges, int n_ranges,
+                                               int hidden, int group, float sm_scale, int flags, int out_fp32,
+                                               void *out, kvq_stream_t stream);
 
 /* ---------------------------------------------------------------- device status
  * Waits for `stream`, then returns KVQ_OK, or KVQ_ERR_TIMEOUT if a bounded

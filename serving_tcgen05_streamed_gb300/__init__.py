@@ -9,4 +9,5 @@ from ._lib import (  # noqa: F401
     packed_kv_attention_causal, packed_kv_attention_mixed, padded_rows, scales_bytes, selftest_wait_timeout, status_str,
     streamed_qkv_proj, streamed_qkv_proj_mixed, streamed_qkv_proj_ex, SECTION_Q, SECTION_KV, version,
     packed_kv_attention_partial, partial_state, PARTIAL_MERGE, PARTIAL_FINAL,
+    packed_kv_attention_partial_static, STATIC_STATE_BYTES, KVQ_ERR_TOO_LARGE,
 )

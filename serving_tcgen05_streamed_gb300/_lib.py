@@ -19,14 +19,15 @@ HEAD_DIM = 128
 ROW_TILE = 128
 MAX_RANGES = 16
 
-KVQ_OK, KVQ_ERR_ARG, KVQ_ERR_ALIGN, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_TIMEOUT = range(6)
+KVQ_OK, KVQ_ERR_ARG, KVQ_ERR_ALIGN, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CUDA, KVQ_ERR_TIMEOUT, KVQ_ERR_TOO_LARGE = range(7)
+STATIC_STATE_BYTES = 16 << 20
 
 #: Every function the header declares.
 EXPORTS = (
     "kvq_status_str", "kvq_version", "kvq_padded_rows", "kvq_codes_bytes", "kvq_scales_bytes",
     "kv_rotate_quant_pack", "kv_unpack", "streamed_qkv_proj", "packed_kv_attention",
     "packed_kv_attention_causal", "streamed_qkv_proj_mixed", "streamed_qkv_proj_ex", "packed_kv_attention_mixed",
-    "packed_kv_attention_partial", "kvq_device_status",
+    "packed_kv_attention_partial", "packed_kv_attention_partial_static", "kvq_device_status",
     "kvq_selftest_wait_timeout",
 )
 
@@ -89,6 +90,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.packed_kv_attention_mixed.argtypes = [P, I64, ctypes.POINTER(_Range), I, I, I, F, I, P, P]
         lib.packed_kv_attention_partial.restype = I
         lib.packed_kv_attention_partial.argtypes = [P, I64, ctypes.POINTER(_Range), I, I, I, F, I, P, P, I, P, P]
+        lib.packed_kv_attention_partial_static.restype = I
+        lib.packed_kv_attention_partial_static.argtypes = [P, I64, ctypes.POINTER(_Range), I, I, I, F, I, I, P, P]
         lib.kvq_device_status.restype = I
         lib.kvq_device_status.argtypes = [P]
         lib.kvq_selftest_wait_timeout.restype = I
@@ -365,6 +368,26 @@ def packed_kv_attention_partial(q: torch.Tensor, stores: list[PackedKV], state=N
                                             _stream(stream))
     _check(st, "packed_kv_attention_partial")
     return out if final else state
+
+
+def packed_kv_attention_partial_static(q: torch.Tensor, stores: list[PackedKV], merge: bool = False,
+                                       final: bool = False, sm_scale: float = 0.0, out_fp32: bool = False,
+                                       out: torch.Tensor | None = None, stream=None):
+    """packed_kv_attention_partial with the carried state in the library's fixed
+    device area (for callers that cannot allocate device memory; at most
+    STATIC_STATE_BYTES of state, one sequence of calls at a time per device).
+    Returns `out` with final=True, else None."""
+    _need_cuda(q)
+    n_q, C = q.shape
+    if final and out is None:
+        out = torch.empty((n_q, C), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)
+    arr = _ranges(stores)
+    flags = (PARTIAL_MERGE if merge else 0) | (PARTIAL_FINAL if final else 0)
+    st = load().packed_kv_attention_partial_static(_ptr(q), n_q, arr, len(stores), C, stores[0].group, sm_scale,
+                                                   flags, int(out_fp32), _ptr(out) if final else None,
+                                                   _stream(stream))
+    _check(st, "packed_kv_attention_partial_static")
+    return out if final else None
 
 
 def device_status(stream=None) -> int:

@@ -155,6 +155,7 @@ const char *kvq_status_str(int status) {
         case KVQ_ERR_UNSUPPORTED: return "unsupported combination";
         case KVQ_ERR_CUDA: return "CUDA error";
         case KVQ_ERR_TIMEOUT: return "device wait timed out";
+        case KVQ_ERR_TOO_LARGE: return "request exceeds the library's fixed state area (KVQ_STATIC_STATE_BYTES)";
         default: return "unknown status";
     }
 }
