@@ -179,6 +179,24 @@ def max_over_ranks(world, v: float) -> float:
     return float(t.item())
 
 
+def timed_leg(step, steps: int, world: int, device_index: int):
+    """Runs E2E_WARMUP untimed steps, then `steps` timed ones (wall clock, each
+    step ends synchronised), sampling the SM clock over the timed region.
+    Returns (seconds per step, max over ranks; clock record)."""
+    for _ in range(E2E_WARMUP):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(device_index)
+    sampler.start()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    secs = (time.perf_counter() - t0) / steps
+    clocks = sampler.stop()
+    return max_over_ranks(world, secs), clocks
+
+
 def job_value(world: int, rank_ms_total: float, steps: int, flops_per_block: float) -> tuple[float, float]:
     """(ms per step, whole-job TFLOP/s): every rank runs one block per step, the
     step time is the slowest rank's."""
@@ -498,14 +516,7 @@ def run_gpu(args, wl, world, rank, local):
         torch.cuda.synchronize()
 
     e2e_steps = max(1, min(args.steps, E2E_STEPS))
-    for i in range(E2E_WARMUP + e2e_steps):
-        if i == E2E_WARMUP:
-            torch.cuda.synchronize()
-            barrier(world)
-            t0 = time.perf_counter()
-        e2e_step()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e_s = max_over_ranks(world, e2e_s)
+    e2e_s, e2e_clocks = timed_leg(e2e_step, e2e_steps, world, local)
     e2e_val = world * (fp + fa) / e2e_s / 1e12
 
     # ------------------------------------------------------------ end to end, two phases (no full Q or output on device)
@@ -562,13 +573,7 @@ def run_gpu(args, wl, world, rank, local):
             ev["out"][b].record(copy)
         torch.cuda.synchronize()
 
-    for i in range(E2E_WARMUP + e2e_steps):
-        if i == E2E_WARMUP:
-            torch.cuda.synchronize()
-            barrier(world)
-            t0 = time.perf_counter()
-        e2e_two_phase_step()
-    e2e2_s = max_over_ranks(world, (time.perf_counter() - t0) / e2e_steps)
+    e2e2_s, e2e2_clocks = timed_leg(e2e_two_phase_step, e2e_steps, world, local)
     peak2_gib = (torch.cuda.max_memory_allocated(dev) - mem0) / GiB
     # device memory the step holds beyond what stays resident across steps (W, norms, table)
     resident_gib = (sum(st_.nbytes() for st_ in stores) + (fine.nbytes() if route else 0)) / GiB
@@ -640,12 +645,12 @@ def run_gpu(args, wl, world, rank, local):
                          "peak_source": f"{peak_kind} bf16 sustained (fp16 dense rate = bf16 dense rate)"},
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(x.numel() * 2),
-                    "d2h_bytes_per_step": int(n * C * 2),
+                    "d2h_bytes_per_step": int(n * C * 2), "ms_per_step": e2e_s * 1e3, "clocks": e2e_clocks,
                     "note": "x copied in from pinned host memory and the attention output copied back each step, "
                             "on a copy stream overlapping the kernels (token chunks in, query chunks out); "
                             "W stays resident"},
             "e2e_two_phase": {"value": world * (fp + fa) / e2e2_s / 1e12, "unit": "TFLOP/s",
-                              "ms_per_step": e2e2_s * 1e3,
+                              "ms_per_step": e2e2_s * 1e3, "clocks": e2e2_clocks,
                               "device_gib": resident_gib + peak2_gib,
                               "device_gib_materialise_bf16_qkv": peak_mat,
                               "h2d_bytes_per_step": int(2 * x.numel() * 2), "d2h_bytes_per_step": int(n * C * 2),
@@ -747,16 +752,10 @@ def host_staged_leg(kvq, wl, w, qn, kn, x_host, out_host, stream, copy, dev, wor
             ev["out"][b].record(copy)
         torch.cuda.synchronize()
 
-    for i in range(E2E_WARMUP + steps):
-        if i == E2E_WARMUP:
-            torch.cuda.synchronize()
-            barrier(world)
-            t0 = time.perf_counter()
-        one_step()
-    secs = max_over_ranks(world, (time.perf_counter() - t0) / steps)
+    secs, clocks = timed_leg(one_step, steps, world, torch.cuda.current_device())
     peak = (torch.cuda.max_memory_allocated(dev) - mem0) / GiB
     store_bytes = sum(t.numel() * t.element_size() for st in host_kv for t in parts(st))
-    return {"unit": "TFLOP/s", "ms_per_step": secs * 1e3, "seconds": secs,
+    return {"unit": "TFLOP/s", "ms_per_step": secs * 1e3, "seconds": secs, "clocks": clocks,
             "device_gib": peak, "host_store_gib": store_bytes / GiB,
             "h2d_bytes_per_step": int(2 * n * C * 2 + len(out_chunks) * store_bytes),
             "d2h_bytes_per_step": int(store_bytes + n * C * 2),

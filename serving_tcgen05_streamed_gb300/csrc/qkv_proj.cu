@@ -13,14 +13,15 @@
 //              each CTA owns 128 of the tokens
 //   warp 0     TMA producer of each CTA: its 128 rows of x and its half (128
 //              rows) of the tile's W rows per stage, 128-byte swizzle,
-//              6-stage shared-memory ring
+//              6-stage shared-memory ring.  The copies of both CTAs complete
+//              on the even CTA's barrier of the stage (the CTA-pair form of
+//              the TMA load), which the even producer arms for both CTAs' bytes.
 //   warp 1     TMEM allocation (jointly with the peer).  In the even CTA the
 //              MMA issuer: tcgen05.mma.cta_group::2 kind::f16 M=256 N=256
 //              K=16 (rows 0-127 from the even CTA, 128-255 from the odd one;
 //              B split along N between the two SMs), fp32 accumulators in each
 //              CTA's TMEM, two 256-column accumulators so the epilogue of one
-//              tile overlaps the main loop of the next.  In the odd CTA it
-//              relays each of its landed stages to the even CTA's barrier.
+//              tile overlaps the main loop of the next.
 //   warps 2-5  epilogue of each CTA on its own 128 rows: one thread per token
 //              row reads a head's 128 fp32 values from TMEM (tcgen05.ld
 //              32x32b), applies RMSNorm (Q, K, optional), the 128-point
@@ -28,9 +29,12 @@
 //              INT8 codes into the head-major store.  The accumulator never
 //              leaves the SM in fp32 or BF16.
 // Tiles are walked chunk by chunk (chunk_tokens rows at a time, rounded up
-// to whole 256-row pair tiles), columns-outer within a chunk, so that a chunk of
-// x and a few W column blocks stay in L2.  Every output element depends only
-// on its token row, so the results do not depend on the chunk size.
+// to whole 256-row pair tiles).  Inside a chunk they go in groups of
+// RASTER_M pair tiles (2048 rows of x, 29 MB), each group sweeping every W
+// column block before the next starts: the group's x stays in L2 while W
+// streams past, and a W block is used by all the group's tiles at once.
+// Every output element depends only on its token row, so the results do not
+// depend on the chunk size or the walk.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,6 +57,10 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* align slack */ + 256 /* barriers */;
+#ifndef KVQ_RASTER_M
+#define KVQ_RASTER_M 8
+#endif
+constexpr int RASTER_M = KVQ_RASTER_M;  // pair tiles of x per group of the tile walk
 
 struct ProjParams {
     int64_t n;
@@ -76,9 +84,15 @@ __device__ __forceinline__ void tile_coords(int64_t T, const ProjParams &p, int 
     const int64_t c = T / per_chunk;
     const int64_t local = T - c * per_chunk;
     const int m0 = static_cast<int>(c) * p.chunk_m_tiles;
-    const int mc = min(p.chunk_m_tiles, p.m_tiles - m0);
-    n_idx = p.col_tile0 + static_cast<int>(local / mc);
-    m_idx = m0 + static_cast<int>(local % mc);
+    const int mc = min(p.chunk_m_tiles, p.m_tiles - m0);  // pair tiles in this chunk
+    const int G = min(RASTER_M, mc);
+    const int64_t per_group = static_cast<int64_t>(G) * p.n_tiles;
+    const int gi = static_cast<int>(local / per_group);   // group inside the chunk (the last may be short)
+    const int64_t lg = local - gi * per_group;
+    const int gm0 = gi * G;
+    const int gmc = min(G, mc - gm0);
+    n_idx = p.col_tile0 + static_cast<int>(lg / gmc);
+    m_idx = m0 + gm0 + static_cast<int>(lg % gmc);
 }
 
 __device__ __forceinline__ void rmsnorm128(float (&v)[128], const float *__restrict__ w, float eps) {
@@ -143,12 +157,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *smem_a = smem;
     uint8_t *smem_b = smem + STAGES * A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);  // this CTA's copies landed
-    uint64_t *peer_full = full + STAGES;  // even CTA: the odd CTA's copies landed
-    uint64_t *empty = peer_full + STAGES;  // both CTAs: the stage's MMAs completed
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);  // even CTA: both CTAs' copies landed
+    uint64_t *empty = full + STAGES;       // both CTAs: the stage's MMAs completed
     uint64_t *tfull = empty + STAGES;      // both CTAs: an accumulator is complete
     uint64_t *tempty = tfull + 2;          // even CTA: both CTAs' epilogues have read an accumulator
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *drain = tempty + 2;          // even CTA: every MMA issued has completed (abort path only)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -157,13 +171,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&peer_full[i], 1);
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], 2 * 4);  // one arrive per epilogue warp of both CTAs
         }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -183,22 +197,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer (both CTAs)
-        // its 128 rows of x and its half (128 rows) of the tile's W rows, into its own ring
+        // its 128 rows of x and its half (128 rows) of the tile's W rows, into its own ring;
+        // both CTAs' copies complete on the even CTA's full barrier of the stage
         if (elect_one()) {
+            const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0;  // bit s: stage s has been armed at least once
             uint32_t armed_parity = 0;
+            bool issued = false;
             for (int64_t T = cluster; T < p.total_tiles && !*abort_flag; T += clusters) {
                 int m_idx, n_idx;
                 tile_coords(T, p, m_idx, n_idx);
                 const int y = (2 * m_idx + static_cast<int>(rank)) * BM;
+                bool ok = true;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_err_proj)) break;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    tma_load_2d(smem_a + stage * A_BYTES, &tm_x, &full[stage], kb * BK, y);
-                    tma_load_2d(smem_b + stage * B_BYTES, &tm_w, &full[stage], kb * BK,
-                                n_idx * BN + static_cast<int>(rank) * BNH);
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_err_proj)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+                    const uint32_t bar = full_leader + stage * 8;
+                    tma_load_2d_pair(smem_a + stage * A_BYTES, &tm_x, bar, kb * BK, y);
+                    tma_load_2d_pair(smem_b + stage * B_BYTES, &tm_w, bar, kb * BK,
+                                     n_idx * BN + static_cast<int>(rank) * BNH);
+                    issued = true;
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -206,36 +229,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                         phase ^= 1u;
                     }
                 }
+                if (!ok) break;
             }
-            // drain: every copy this thread started has landed before the CTA exits
+            // drain: every copy this thread started has landed before the CTA exits.  The even
+            // CTA waits on its barriers, which count both CTAs' bytes; it reaches the final
+            // cluster barrier, and with it lets the odd CTA leave, only after that.  An odd CTA
+            // that gave up (a wait ran out) cannot see the even CTA's barriers: it gives its
+            // copies in flight a bounded grace period instead.
             volatile int no_abort = 0;
-            for (int s = 0; s < STAGES; ++s)
-                if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &no_abort, nullptr);
+            if (rank == 0) {
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1u, &no_abort, nullptr);
+            } else if (issued && *abort_flag) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 100000ull) {
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (rank == 1) {
-            // ------------------------------------------------------ odd CTA: relay of its landed stages
-            if (elect_one()) {
-                const uint32_t peer = mapa_shared(smem_u32(peer_full), 0);
-                int stage = 0;
-                uint32_t phase = 0;
-                for (int64_t T = cluster; T < p.total_tiles && !*abort_flag; T += clusters) {
-                    bool ok = true;
-                    for (int kb = 0; kb < p.k_blocks; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag, &g_err_proj)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_cluster(peer + stage * 8);
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                }
-            }
+            // the odd CTA's MMA warp has nothing to issue: the even CTA's MMAs read its stages
         } else if (elect_one()) {
             // ------------------------------------------------------ even CTA: MMA issuer for the pair
             constexpr uint32_t idesc = make_idesc_f16(2 * BM, BN, 1);
@@ -250,8 +264,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 bool ok = true;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, &g_err_proj) ||
-                        !mbar_wait_cluster(&peer_full[stage], phase, abort_flag, &g_err_proj)) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, &g_err_proj)) {  // both CTAs' bytes
                         ok = false;
                         break;
                     }
@@ -276,11 +289,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 if (acc == 0) acc_phase ^= 1u;
             }
             if (issued && *abort_flag) {
-                // drain: every MMA issued so far has completed before the pair tears down
+                // drain: every MMA issued so far has completed before the pair tears down;
+                // on a barrier of its own, so no epilogue takes a partial accumulator as complete
                 volatile int no_abort = 0;
-                uint64_t *drain = &tfull[acc];
                 mma_commit_pair(drain, 0x1);
-                mbar_wait(drain, acc_phase, &no_abort, nullptr, 1000000000ull);
+                mbar_wait(drain, 0, &no_abort, nullptr, 1000000000ull);
             }
         }
         __syncwarp();
@@ -298,6 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             m_idx = 2 * m_idx + static_cast<int>(rank);  // this CTA's 128-row tile of the pair's 256
             // warp-uniform before the warp-collective TMEM loads
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, &g_err_proj))) break;
+            if (__any_sync(0xffffffffu, *abort_flag)) break;  // a wait elsewhere ran out: store nothing more
             tc_fence_after();
             const int64_t row = static_cast<int64_t>(m_idx) * BM + quarter * 32 + lane;
 #pragma unroll 1
