@@ -19,7 +19,9 @@ itself in host memory, streamed back chunk by chunk into a key-chunked
 attention (e2e_host_staged), the standalone rotate + quantise + pack kernel
 and its inverse on K/V [262,144, 2 x 7168] (kernels.pack), the peak memory
 against materialising the BF16 QKV, and the CPU oracle's time on a sample
-(cpu_baseline).
+(cpu_baseline).  Each end-to-end leg records its own SM clocks and the rate
+its copies got from the host link (host_link, CUDA events around each copy):
+that rate differs from box to box and over time, and the legs depend on it.
 
 --impl reference times the CPU oracle (the plain C reference implementation
 of the same computation) on a bounded sample of the same workload.
@@ -143,6 +145,39 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class LinkMeter:
+    """Times each host<->device copy of an end-to-end leg with a pair of CUDA
+    events on the copy's own stream (recorded after any wait the stream was
+    given, so only the copy itself is timed), and reports the rate the host
+    link delivered in each direction over the timed steps."""
+
+    def __init__(self):
+        self.pending = []
+        self.reset()
+
+    def reset(self):
+        self.pending.clear()
+        self.bytes = {"h2d": 0, "d2h": 0}
+        self.ms = {"h2d": 0.0, "d2h": 0.0}
+
+    def copy(self, dst, src, s, kind: str):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            dst.copy_(src, non_blocking=True)
+            b.record(s)
+        self.pending.append((kind, a, b, dst.numel() * dst.element_size()))
+
+    def collect(self):  # after a synchronize
+        for kind, a, b, nb in self.pending:
+            self.ms[kind] += a.elapsed_time(b)
+            self.bytes[kind] += nb
+        self.pending.clear()
+
+    def record(self) -> dict:
+        return {k + "_gbs": (self.bytes[k] / (self.ms[k] * 1e6) if self.ms[k] > 0 else None) for k in ("h2d", "d2h")}
+
+
 def dist_setup(gpus: int, backend: str = "nccl"):
     """One process per GPU (torchrun): returns (world, rank, local_rank).
     Every rank runs its own independent block; the process group is used only
@@ -179,13 +214,16 @@ def max_over_ranks(world, v: float) -> float:
     return float(t.item())
 
 
-def timed_leg(step, steps: int, world: int, device_index: int):
+def timed_leg(step, steps: int, world: int, device_index: int, meter: LinkMeter | None = None):
     """Runs E2E_WARMUP untimed steps, then `steps` timed ones (wall clock, each
-    step ends synchronised), sampling the SM clock over the timed region.
+    step ends synchronised), sampling the SM clock over the timed region; the
+    meter, if any, keeps the copies of the timed steps only.
     Returns (seconds per step, max over ranks; clock record)."""
     for _ in range(E2E_WARMUP):
         step()
     torch.cuda.synchronize()
+    if meter is not None:
+        meter.reset()
     barrier(world)
     sampler = ClockSampler(device_index)
     sampler.start()
@@ -194,6 +232,8 @@ def timed_leg(step, steps: int, world: int, device_index: int):
         step()
     secs = (time.perf_counter() - t0) / steps
     clocks = sampler.stop()
+    if meter is not None:
+        meter.collect()
     return max_over_ranks(world, secs), clocks
 
 
@@ -488,12 +528,11 @@ def run_gpu(args, wl, world, rank, local):
 
     def e2e_step():
         landed = []
-        with torch.cuda.stream(copy):
-            for s0, ln in in_chunks:
-                x_dev[s0:s0 + ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(copy)
-                landed.append(ev)
+        for s0, ln in in_chunks:
+            link.copy(x_dev[s0:s0 + ln], x_host[s0:s0 + ln], copy, "h2d")
+            ev = torch.cuda.Event()
+            ev.record(copy)
+            landed.append(ev)
         for (s0, ln), ev in zip(in_chunks, landed):
             stream.wait_event(ev)
             if rope is not None:
@@ -511,12 +550,13 @@ def run_gpu(args, wl, world, rank, local):
             ev = torch.cuda.Event()
             ev.record(stream)
             copy.wait_event(ev)
-            with torch.cuda.stream(copy):
-                out_host[s0:s0 + ln].copy_(qc, non_blocking=True)
+            link.copy(out_host[s0:s0 + ln], qc, copy, "d2h")
         torch.cuda.synchronize()
 
     e2e_steps = max(1, min(args.steps, E2E_STEPS))
-    e2e_s, e2e_clocks = timed_leg(e2e_step, e2e_steps, world, local)
+    link = LinkMeter()
+    e2e_s, e2e_clocks = timed_leg(e2e_step, e2e_steps, world, local, link)
+    e2e_link = link.record()
     e2e_val = world * (fp + fa) / e2e_s / 1e12
 
     # ------------------------------------------------------------ end to end, two phases (no full Q or output on device)
@@ -538,8 +578,7 @@ def run_gpu(args, wl, world, rank, local):
         for i, (s0, ln) in enumerate(in_chunks):
             b = i % 2
             copy.wait_event(ev["p1"][b])  # chunk i-2's projection has read xb[b]
-            with torch.cuda.stream(copy):
-                xb[b][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+            link.copy(xb[b][:ln], x_host[s0:s0 + ln], copy, "h2d")
             ev["in1"][b].record(copy)
             stream.wait_event(ev["in1"][b])
             kvq.streamed_qkv_proj_ex(xb[b][:ln], w, windows(s0, ln), rope[s0:s0 + ln] if rope is not None else None,
@@ -550,8 +589,7 @@ def run_gpu(args, wl, world, rank, local):
         for i, (s0, ln) in enumerate(out_chunks):
             b = i % 2
             if i == 0:
-                with torch.cuda.stream(copy):
-                    xq[0][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+                link.copy(xq[0][:ln], x_host[s0:s0 + ln], copy, "h2d")
                 ev["in2"][0].record(copy)
             stream.wait_event(ev["in2"][b])
             stream.wait_event(ev["out"][b])  # chunk i-2's output has left qb[b]
@@ -564,16 +602,16 @@ def run_gpu(args, wl, world, rank, local):
             if i + 1 < len(out_chunks):  # next chunk's x, once the projection of chunk i-1 has read xq[1-b]
                 s1, l1 = out_chunks[i + 1]
                 copy.wait_event(ev["qp"][1 - b])
-                with torch.cuda.stream(copy):
-                    xq[1 - b][:l1].copy_(x_host[s1:s1 + l1], non_blocking=True)
+                link.copy(xq[1 - b][:l1], x_host[s1:s1 + l1], copy, "h2d")
                 ev["in2"][1 - b].record(copy)
             copy.wait_event(ev["attn"][b])
-            with torch.cuda.stream(copy):
-                out_host[s0:s0 + ln].copy_(qc, non_blocking=True)
+            link.copy(out_host[s0:s0 + ln], qc, copy, "d2h")
             ev["out"][b].record(copy)
         torch.cuda.synchronize()
 
-    e2e2_s, e2e2_clocks = timed_leg(e2e_two_phase_step, e2e_steps, world, local)
+    link = LinkMeter()
+    e2e2_s, e2e2_clocks = timed_leg(e2e_two_phase_step, e2e_steps, world, local, link)
+    e2e2_link = link.record()
     peak2_gib = (torch.cuda.max_memory_allocated(dev) - mem0) / GiB
     # device memory the step holds beyond what stays resident across steps (W, norms, table)
     resident_gib = (sum(st_.nbytes() for st_ in stores) + (fine.nbytes() if route else 0)) / GiB
@@ -646,11 +684,12 @@ def run_gpu(args, wl, world, rank, local):
             "clocks": clocks,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(x.numel() * 2),
                     "d2h_bytes_per_step": int(n * C * 2), "ms_per_step": e2e_s * 1e3, "clocks": e2e_clocks,
+                    "host_link": e2e_link,
                     "note": "x copied in from pinned host memory and the attention output copied back each step, "
                             "on a copy stream overlapping the kernels (token chunks in, query chunks out); "
                             "W stays resident"},
             "e2e_two_phase": {"value": world * (fp + fa) / e2e2_s / 1e12, "unit": "TFLOP/s",
-                              "ms_per_step": e2e2_s * 1e3, "clocks": e2e2_clocks,
+                              "ms_per_step": e2e2_s * 1e3, "clocks": e2e2_clocks, "host_link": e2e2_link,
                               "device_gib": resident_gib + peak2_gib,
                               "device_gib_materialise_bf16_qkv": peak_mat,
                               "h2d_bytes_per_step": int(2 * x.numel() * 2), "d2h_bytes_per_step": int(n * C * 2),
@@ -692,6 +731,10 @@ def host_staged_leg(kvq, wl, w, qn, kn, x_host, out_host, stream, copy, dev, wor
     xq = [torch.empty((E2E_OUT_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     qb = [torch.empty((E2E_OUT_CHUNK, C), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     o_acc, lse_acc = kvq.partial_state(E2E_OUT_CHUNK, C, dev)
+    # device-to-host copies get a stream of their own: on the copy stream, a chunk's
+    # store or output waiting for its kernel would hold up the next x chunk or key
+    # chunk queued behind it
+    copy_out = torch.cuda.Stream(device=dev)
     ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in1", "p1", "kvout", "in2", "qp", "kvin", "attn",
                                                               "out")}
     parts = lambda st: (st.k_codes, st.v_codes, st.k_scales, st.v_scales)  # noqa: E731
@@ -700,25 +743,23 @@ def host_staged_leg(kvq, wl, w, qn, kn, x_host, out_host, stream, copy, dev, wor
         for i, (s0, ln) in enumerate(kv_chunks):  # phase 1: K/V of every token, to the host
             b = i % 2
             copy.wait_event(ev["p1"][b])
-            with torch.cuda.stream(copy):
-                xb[b][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+            link.copy(xb[b][:ln], x_host[s0:s0 + ln], copy, "h2d")
             ev["in1"][b].record(copy)
             stream.wait_event(ev["in1"][b])
             stream.wait_event(ev["kvout"][b])  # the chunk store of chunk i-2 has gone to the host
             kvq.streamed_qkv_proj_ex(xb[b][:ln], w, [kv_dev[b].rows(0, ln)], sections=kvq.SECTION_KV, group=32,
                                      chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn, stream=stream)
             ev["p1"][b].record(stream)
-            copy.wait_event(ev["p1"][b])
-            with torch.cuda.stream(copy):
-                for d, s_ in zip(parts(host_kv[i]), parts(kv_dev[b])):
-                    d.copy_(s_, non_blocking=True)
-            ev["kvout"][b].record(copy)
+            copy_out.wait_event(ev["p1"][b])
+            for d, s_ in zip(parts(host_kv[i]), parts(kv_dev[b])):
+                link.copy(d, s_, copy_out, "d2h")
+            ev["kvout"][b].record(copy_out)
+        copy.wait_stream(copy_out)  # the key chunks go back to the device buffers only once they have all left
         kc = 0
         for i, (s0, ln) in enumerate(out_chunks):  # phase 2: Q per query chunk, the store streamed in
             b = i % 2
             if i == 0:
-                with torch.cuda.stream(copy):
-                    xq[0][:ln].copy_(x_host[s0:s0 + ln], non_blocking=True)
+                link.copy(xq[0][:ln], x_host[s0:s0 + ln], copy, "h2d")
                 ev["in2"][0].record(copy)
             stream.wait_event(ev["in2"][b])
             stream.wait_event(ev["out"][b])
@@ -729,33 +770,32 @@ def host_staged_leg(kvq, wl, w, qn, kn, x_host, out_host, stream, copy, dev, wor
             if i + 1 < len(out_chunks):  # next chunk's x, once the projection of chunk i-1 has read it
                 s1, l1 = out_chunks[i + 1]
                 copy.wait_event(ev["qp"][1 - b])
-                with torch.cuda.stream(copy):
-                    xq[1 - b][:l1].copy_(x_host[s1:s1 + l1], non_blocking=True)
+                link.copy(xq[1 - b][:l1], x_host[s1:s1 + l1], copy, "h2d")
                 ev["in2"][1 - b].record(copy)
             state = (o_acc[:ln], lse_acc[:ln])
             for j, (k0, kl) in enumerate(kv_chunks):
                 kb = kc % 2
                 kc += 1
                 copy.wait_event(ev["attn"][kb])  # the attention that last read this buffer has run
-                with torch.cuda.stream(copy):
-                    for d, s_ in zip(parts(kv_dev[kb]), parts(host_kv[j])):
-                        d.copy_(s_, non_blocking=True)
+                for d, s_ in zip(parts(kv_dev[kb]), parts(host_kv[j])):
+                    link.copy(d, s_, copy, "h2d")
                 ev["kvin"][kb].record(copy)
                 stream.wait_event(ev["kvin"][kb])
                 last = j == len(kv_chunks) - 1
                 kvq.packed_kv_attention_partial(qc, [kv_dev[kb].rows(0, kl)], state=state, merge=j > 0, final=last,
                                                 out=qc if last else None, stream=stream)
                 ev["attn"][kb].record(stream)
-            copy.wait_event(ev["attn"][(kc - 1) % 2])
-            with torch.cuda.stream(copy):
-                out_host[s0:s0 + ln].copy_(qc, non_blocking=True)
-            ev["out"][b].record(copy)
+            copy_out.wait_event(ev["attn"][(kc - 1) % 2])
+            link.copy(out_host[s0:s0 + ln], qc, copy_out, "d2h")
+            ev["out"][b].record(copy_out)
         torch.cuda.synchronize()
 
-    secs, clocks = timed_leg(one_step, steps, world, torch.cuda.current_device())
+    link = LinkMeter()
+    secs, clocks = timed_leg(one_step, steps, world, torch.cuda.current_device(), link)
     peak = (torch.cuda.max_memory_allocated(dev) - mem0) / GiB
     store_bytes = sum(t.numel() * t.element_size() for st in host_kv for t in parts(st))
     return {"unit": "TFLOP/s", "ms_per_step": secs * 1e3, "seconds": secs, "clocks": clocks,
+            "host_link": link.record(),
             "device_gib": peak, "host_store_gib": store_bytes / GiB,
             "h2d_bytes_per_step": int(2 * n * C * 2 + len(out_chunks) * store_bytes),
             "d2h_bytes_per_step": int(store_bytes + n * C * 2),
