@@ -28,8 +28,11 @@ def _check_store(store, kv_cpu, hidden, group, bits, rows=None):
 
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("group", [32, 64, 128])
-@pytest.mark.parametrize("n,hidden", [(1000, 1024), (1, 256), (129, 384)])
+@pytest.mark.parametrize("n,hidden", [(1000, 1024), (1, 256), (129, 384), (7, 256), (127, 256), (128, 256),
+                                      (255, 256)])
 def test_pack_bit_exact(n, hidden, group, bits):
+    # a block of the kernel covers 128 tokens in 16 passes of 8 and prefetches the next
+    # pass's rows: sizes below, at and past one block and one pass, with ragged tails
     kv = inputs.sweep_kv(n, hidden, seed=n + group + bits)
     store = kvq.kv_rotate_quant_pack(kv.cuda(), hidden, group, bits)
     torch.cuda.synchronize()
@@ -81,8 +84,9 @@ def test_pack_sweep_max_size_sampled(group):
 
 @pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("group", [32, 64])
-def test_unpack_bit_exact(group, bits):
-    n, C = 333, 768
+@pytest.mark.parametrize("n", [333, 9, 128])
+def test_unpack_bit_exact(group, bits, n):
+    C = 768
     kv = inputs.sweep_kv(n, C, seed=7)
     store = kvq.kv_rotate_quant_pack(kv.cuda(), C, group, bits)
     out = kvq.kv_unpack(store, C)
