@@ -76,7 +76,10 @@ def test_fuzz_pack(seed):
     assert np.array_equal(to_token_major(store.v_scales, rows).view(np.uint16), vs)
     for t in (store.k_codes, store.v_codes, store.k_scales, store.v_scales):
         assert int(t[:, n:].view(torch.uint8).count_nonzero()) == 0
-    out = kvq.kv_unpack(store, C)
+    # the output with the same padded row stride: 32-byte aligned rows take the 32-byte stores,
+    # others the interleaved 16-byte form
+    wide_out = torch.empty((n, 2 * C + pad), dtype=torch.bfloat16, device="cuda")
+    out = kvq.kv_unpack(store, C, out=wide_out[:, :2 * C])
     torch.cuda.synchronize()
     assert np.array_equal(bits16(out), oracle.kv_unpack(kc, vc, ks, vs, group=group, bits=bits))
 

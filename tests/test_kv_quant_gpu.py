@@ -96,6 +96,22 @@ def test_unpack_bit_exact(group, bits, n):
     assert np.array_equal(bits16(out), ref)
 
 
+@pytest.mark.parametrize("pad", [0, 8, 16])
+def test_pack_and_unpack_strided_rows(pad):
+    # rows of 2C + pad BF16: pad 0 and 16 keep them 32-byte aligned (32-byte loads and
+    # stores), pad 8 does not (16-byte forms); all give the same bits
+    n, C = 300, 512
+    kv = inputs.sweep_kv(n, C, seed=11)
+    wide_in = torch.zeros((n, 2 * C + pad), dtype=torch.bfloat16)
+    wide_in[:, :2 * C] = kv
+    store = kvq.kv_rotate_quant_pack(wide_in.cuda()[:, :2 * C], C, 32, 8)
+    wide_out = torch.empty((n, 2 * C + pad), dtype=torch.bfloat16, device="cuda")
+    out = kvq.kv_unpack(store, C, out=wide_out[:, :2 * C])
+    torch.cuda.synchronize()
+    kc, vc, ks, vs = _check_store(store, kv, C, 32, 8)
+    assert np.array_equal(bits16(out), oracle.kv_unpack(kc, vc, ks, vs, group=32, bits=8))
+
+
 def test_pack_is_deterministic_and_stream_ordered():
     n, C = 2048, 1024
     kv = inputs.sweep_kv(n, C, seed=9).cuda()
