@@ -8,22 +8,24 @@
 //
 // Both kernels are HBM-bound: per token they move 2*hidden*2 bytes of BF16
 // and 2*hidden*(bits/8 + 2/group) bytes of codes and scales.  Four lanes own
-// one 128-wide head vector.  In the pack kernel they hold 32 consecutive
-// elements each, so five of the seven butterfly stages and (for groups of 32)
-// the whole group absmax stay inside a lane, and a lane's codes leave in one
-// 16-byte store; the unpack kernel interleaves them (see there).  A warp works on 8
-// tokens of one head slot at a time (K heads, then V heads); a block of 8
-// warps covers 8 head slots x 128 tokens in 16 passes.  The pack kernel is
-// held to 64 registers, so four blocks (32 warps) share an SM: one pass of 8
-// tokens at a time fits (ptxas reports one 8-byte spill store), and this
-// measured 1.5-4 % faster than two passes loaded ahead at 80
+// one 128-wide head vector, 32 consecutive elements each, so five of the
+// seven butterfly stages and (for groups of 32) the whole group absmax stay
+// inside a lane, and a lane's codes leave in one 16-byte store (the unpack
+// has an interleaved form for unaligned outputs, see there).  A warp works on
+// 8 tokens of one head slot at a time (K heads, then V heads); a block of 8
+// warps covers 8 head slots x 128 tokens in 16 passes.
+//
+// The pack kernel is held to 64 registers, so four blocks (32 warps) share an
+// SM: one pass of 8 tokens at a time fits (ptxas reports one 8-byte spill
+// store), and this measured 1.5-4 % faster than two passes loaded ahead at 80
 // registers, 3 blocks / SM.  Instead of registers, each pass asks L2 for the
 // next pass's rows (prefetch.global.L2, one instruction per warp, no register
 // held), so the next pass's loads find their lines on chip: +10 % for the
 // pack kernel, +3 % for unpack (N = 262,144, same codes).  Blocks of 32 tokens
 // left a quarter of the passes without a prefetch; blocks longer than 128
 // tokens measured slower.  The stride-1 butterfly reads the BF16 halves
-// directly (+1 %).
+// directly (+1 %).  Global accesses move whole 32-byte sectors where the
+// alignment allows (32-byte loads and stores, sm_100 and later).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
