@@ -108,14 +108,18 @@ KVQ_API size_t kvq_scales_bytes(int64_t cap, int hidden, int group);
  * kv: BF16 [n][ld_kv] device; K = columns [0, hidden), V = [hidden, 2*hidden).
  * Writes the K and V stores (cap = kvq_padded_rows(n), pad rows zeroed).
  * group in {32, 64, 128}; bits in {4, 8}.  ld_kv >= 2*hidden, a multiple of 8.
- * Codes and scales are bit-exact with the conventions above. */
+ * Codes and scales are bit-exact with the conventions above.  Rows and code
+ * arrays on 32-byte boundaries (kv, ld_kv * 2, k_codes, v_codes) take 32-byte
+ * loads and stores, which run faster; other valid layouts give the same bytes. */
 KVQ_API int kv_rotate_quant_pack(const void *kv, int64_t n, int hidden, int64_t ld_kv, int group, int bits, void *k_codes,
                          void *v_codes, void *k_scales, void *v_scales, kvq_stream_t stream);
 
 /* ---------------------------------------------------------------- a1b: unpack (diagnostic)
  * Inverse of a1: dequantise (code * float(s)), un-rotate, round to BF16 into
  * kv_out [n][ld_out] (K then V, as a1's input).  This materialises BF16 K/V
- * by design; the attention never calls it. */
+ * by design; the attention never calls it.  An output on 32-byte boundaries
+ * (kv_out, ld_out * 2) takes 32-byte stores, which run faster; other valid
+ * layouts give the same bytes. */
 KVQ_API int kv_unpack(const void *k_codes, const void *v_codes, const void *k_scales, const void *v_scales, int64_t n,
               int hidden, int group, int bits, void *kv_out, int64_t ld_out, kvq_stream_t stream);
 
