@@ -429,12 +429,13 @@ __device__ __forceinline__ bool decode_tile(const uint8_t *stg_k, const uint8_t 
     return v_free || __all_sync(0xffffffffu, mbar_wait(v_empty, ph, abort_flag, &g_err_attn));
 }
 
-// First query row of this CTA.  Causal: CTA pairs in reverse order, the longest
-// first.  Recomputed where needed (from special registers) rather than kept live.
+// First query row of this CTA, recomputed where needed (from a special
+// register) rather than kept live.  Causal pairs go in row order too: running
+// them longest first (reversed) measured 0.7 % slower at N = 152,263, with
+// every head's pairs dispatched one head after another either way.
 template <bool CAUSAL>
 __device__ __forceinline__ int64_t cta_row0() {
-    const int64_t x = blockIdx.x;
-    return CAUSAL ? (static_cast<int64_t>(gridDim.x) - 2 - (x & ~int64_t(1)) + (x & 1)) * BQ : x * BQ;
+    return static_cast<int64_t>(blockIdx.x) * BQ;
 }
 // Key tiles this CTA pair walks: all of them, or (causal) those up to the
 // position of the pair's last query row; both CTAs of a pair get the same count.
