@@ -17,8 +17,8 @@
 //
 // The pack kernel is held to 64 registers, so four blocks (32 warps) share an
 // SM: one pass of 8 tokens at a time fits (ptxas reports one 8-byte spill
-// store), and this measured 1.5-4 % faster than two passes loaded ahead at 80
-// registers, 3 blocks / SM.  Instead of registers, each pass asks L2 for the
+// store in the INT8 forms), and this measured 1.5-4 % faster than two passes
+// loaded ahead at 80 registers, 3 blocks / SM.  Instead of registers, each pass asks L2 for the
 // next pass's rows (prefetch.global.L2, one instruction per warp, no register
 // held), so the next pass's loads find their lines on chip: +10 % for the
 // pack kernel, +3 % for unpack (N = 262,144, same codes).  Blocks of 32 tokens
