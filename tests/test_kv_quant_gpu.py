@@ -66,20 +66,26 @@ def test_pack_h3_width_full():
     _check_store(store, kv, C, 32, 4)
 
 
-@pytest.mark.parametrize("group", [32, 128])
-def test_pack_sweep_max_size_sampled(group):
+@pytest.mark.parametrize("group,bits", [(32, 4), (128, 4), (64, 8), (128, 8)])
+def test_pack_sweep_max_size_sampled(group, bits):
     # the largest sweep size, N = 262,144, sampled rows (rows are independent)
     n, C = 262144, 7168
     kv = inputs.sweep_kv(n, C, seed=2, device="cuda")
-    store = kvq.kv_rotate_quant_pack(kv, C, group, 4)
+    store = kvq.kv_rotate_quant_pack(kv, C, group, bits)
     torch.cuda.synchronize()
     rows = inputs.sample_rows(n, 256, seed=3).numpy()
     kc, vc, ks, vs = oracle.kv_rotate_quant_pack(bits16(kv[torch.as_tensor(rows, device="cuda")]), hidden=C,
-                                                 group=group, bits=4)
+                                                 group=group, bits=bits)
     assert np.array_equal(to_token_major(store.k_codes, rows), kc)
     assert np.array_equal(to_token_major(store.v_codes, rows), vc)
     assert np.array_equal(to_token_major(store.k_scales, rows).view(np.uint16), ks)
     assert np.array_equal(to_token_major(store.v_scales, rows).view(np.uint16), vs)
+    # and back: the unpack of the whole store, the same sampled rows
+    del kv
+    out = kvq.kv_unpack(store, C)
+    torch.cuda.synchronize()
+    got = bits16(out[torch.as_tensor(rows, device="cuda")])
+    assert np.array_equal(got, oracle.kv_unpack(kc, vc, ks, vs, group=group, bits=bits))
 
 
 @pytest.mark.parametrize("bits", [4, 8])
