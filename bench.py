@@ -237,6 +237,25 @@ def timed_leg(step, steps: int, world: int, device_index: int, meter: LinkMeter 
     return max_over_ranks(world, secs), clocks
 
 
+def query_chunks(n: int, tail: int = 2048) -> list[tuple[int, int]]:
+    """Query-row chunks of the end-to-end legs: E2E_OUT_CHUNK rows each, then
+    the rest in halving pieces (multiples of 256 rows) down to at most `tail`
+    rows, so that the copy of the last chunk's output, which no attention
+    overlaps, stays small.  Returns (first row, rows) pairs tiling [0, n)."""
+    out, s0 = [], 0
+    while s0 < n:
+        rest = n - s0
+        if rest >= 2 * E2E_OUT_CHUNK:
+            ln = E2E_OUT_CHUNK
+        elif rest <= tail:
+            ln = rest
+        else:
+            ln = min(E2E_OUT_CHUNK, (rest // 2 + 255) // 256 * 256)
+        out.append((s0, ln))
+        s0 += ln
+    return out
+
+
 def job_value(world: int, rank_ms_total: float, steps: int, flops_per_block: float) -> tuple[float, float]:
     """(ms per step, whole-job TFLOP/s): every rank runs one block per step, the
     step time is the slowest rank's."""
@@ -515,7 +534,7 @@ def run_gpu(args, wl, world, rank, local):
     x_dev = torch.empty_like(x)
     copy = torch.cuda.Stream(device=dev)
     in_chunks = [(s0, min(E2E_IN_CHUNK, n - s0)) for s0 in range(0, n, E2E_IN_CHUNK)]
-    out_chunks = [(s0, min(E2E_OUT_CHUNK, n - s0)) for s0 in range(0, n, E2E_OUT_CHUNK)]
+    out_chunks = query_chunks(n)
 
     def windows(s0, length):  # the stores' rows of tokens s0 .. s0+length-1, in order
         out, start = [], 0

@@ -42,3 +42,13 @@ def test_cpu_baseline_record_on_the_tiny_block():
     assert rec["value"] > 0 and rec["single_core"]["value"] > 0
     assert abs(rec["block_s_extrapolated"] - (rec["s_per_projection_row"] + rec["s_per_query_row"]) * 1024) < 1e-9
     assert isinstance(rec["cpu_model"], str) and rec["cpu_model"]
+
+
+def test_query_chunks_tile_the_rows_and_end_small():
+    b = _bench()
+    for n in (1, 255, 2048, 2049, 19456, 40000, 152263, 217088):
+        ch = b.query_chunks(n)
+        assert ch[0][0] == 0 and sum(ln for _, ln in ch) == n
+        assert all(a + ln == c for (a, ln), (c, _) in zip(ch, ch[1:]))
+        assert all(0 < ln <= b.E2E_OUT_CHUNK for _, ln in ch)
+        assert ch[-1][1] <= 2048 or n <= 2048
