@@ -46,6 +46,7 @@ import torch  # noqa: E402
 
 E2E_IN_CHUNK = 16384   # tokens per host-to-device chunk of x in the end-to-end step
 E2E_OUT_CHUNK = 19456  # query rows per attention launch in the end-to-end step (38 CTA pairs)
+E2E_EARLY_QUERY_CHUNKS = 1  # query chunks of the end-to-end step attended while x is still arriving
 E2E_KV_CHUNK = 16384   # keys per host-staged chunk of the packed store
 E2E_STEPS, E2E_WARMUP = 10, 2  # end-to-end steps timed (at most --steps), after these untimed ones
 PACK_N = 262144        # the standalone pack / unpack record: K/V [N, 2 x 7168], group 32
@@ -545,6 +546,16 @@ def run_gpu(args, wl, world, rank, local):
             start += st_.n
         return out
 
+    # While x is still arriving, the first query chunks (their own rows already
+    # projected) attend each newly projected key range through the key-chunk call,
+    # carrying a log-sum-exp state; their last call, once every x chunk is in, writes
+    # their output.  On a slow host link this fills the time the projection would wait
+    # for x.  The other query chunks then attend all keys in one call each.  Not for
+    # the causal and the routed blocks (key-chunk calls are unmasked, one store set).
+    early = out_chunks[:E2E_EARLY_QUERY_CHUNKS] if not causal and not route else []
+    early_rows = early[-1][0] + early[-1][1] if early else 0
+    early_states = [kvq.partial_state(ln, C, dev) for _, ln in early]
+
     def e2e_step():
         landed = []
         for s0, ln in in_chunks:
@@ -552,7 +563,8 @@ def run_gpu(args, wl, world, rank, local):
             ev = torch.cuda.Event()
             ev.record(copy)
             landed.append(ev)
-        for (s0, ln), ev in zip(in_chunks, landed):
+        done = 0  # keys the early query chunks have attended
+        for i, ((s0, ln), ev) in enumerate(zip(in_chunks, landed)):
             stream.wait_event(ev)
             if rope is not None:
                 kvq.streamed_qkv_proj_ex(x_dev[s0:s0 + ln], w, windows(s0, ln), rope[s0:s0 + ln], group=32,
@@ -563,7 +575,21 @@ def run_gpu(args, wl, world, rank, local):
                                             chunk_tokens=wl.chunk_tokens, q_norm_w=qn, k_norm_w=kn,
                                             q_out=q[s0:s0 + ln], stream=stream)
             project_fine(x_dev[s0:s0 + ln], s0, ln)
-        for s0, ln in out_chunks:
+            avail = s0 + ln  # keys projected so far
+            if early and avail >= early_rows and i + 1 < len(in_chunks):
+                for (e0, el), (oa, la) in zip(early, early_states):
+                    kvq.packed_kv_attention_partial(q[e0:e0 + el], windows(done, avail - done), state=(oa, la),
+                                                    merge=done > 0, stream=stream)
+                done = avail
+        for (e0, el), (oa, la) in zip(early, early_states):
+            qc = q[e0:e0 + el]
+            kvq.packed_kv_attention_partial(qc, windows(done, n - done), state=(oa, la), merge=done > 0, final=True,
+                                            out=qc, stream=stream)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            copy.wait_event(ev)
+            link.copy(out_host[e0:e0 + el], qc, copy, "d2h")
+        for s0, ln in out_chunks[len(early):]:
             qc = q[s0:s0 + ln]
             attend_rows(qc, s0)
             ev = torch.cuda.Event()
@@ -705,8 +731,9 @@ def run_gpu(args, wl, world, rank, local):
                     "d2h_bytes_per_step": int(n * C * 2), "ms_per_step": e2e_s * 1e3, "clocks": e2e_clocks,
                     "host_link": e2e_link,
                     "note": "x copied in from pinned host memory and the attention output copied back each step, "
-                            "on a copy stream overlapping the kernels (token chunks in, query chunks out); "
-                            "W stays resident"},
+                            "on a copy stream overlapping the kernels (token chunks in, query chunks out); the "
+                            f"first {len(early)} query chunks attend each key range as it is projected (key-chunk "
+                            "calls with a log-sum-exp state), the rest attend all keys at once; W stays resident"},
             "e2e_two_phase": {"value": world * (fp + fa) / e2e2_s / 1e12, "unit": "TFLOP/s",
                               "ms_per_step": e2e2_s * 1e3, "clocks": e2e2_clocks, "host_link": e2e2_link,
                               "device_gib": resident_gib + peak2_gib,
