@@ -528,8 +528,10 @@ def run_gpu(args, wl, world, rank, local):
     # The copies run on their own stream and overlap the kernels: x goes in by token
     # chunks, each chunk projected (through a row window of the store) as soon as it
     # has landed; the attention runs by query chunks, each chunk's output copied back
-    # while the next is computed.  Results are those of the one-call path (rows are
-    # independent in the projection; the attention does not depend on query tiling).
+    # while the next is computed.  The projection gives the one-call bits (rows are
+    # independent) and so do the query chunks attended in one call; the first query
+    # chunk, attended key range by key range while x arrives (below), differs from
+    # them by the rounding of the log-sum-exp merges, within the attention's bar.
     x_host = x.cpu().pin_memory()
     out_host = torch.empty((n, C), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(x)
